@@ -1,0 +1,66 @@
+"""Each plausible slip in the oracle must be caught by at least one pin.
+
+The oracle source is copied, one mistake is planted by text substitution, the
+copy is compiled with gcc into a temporary directory, and the whole pin suite
+(tests/oracle_pins.py) is run against it.  CPU only; the committed oracle is
+never modified.
+"""
+import ctypes
+import os
+import subprocess
+import sys
+
+import pytest
+
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+import oracle  # noqa: E402
+import oracle_pins as P  # noqa: E402
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle",
+                   "retopk_oracle.c")
+
+MUTANTS = {
+    "no_sqrt_d_scale": ("double inv = 1.0 / sqrt((double)d);", "double inv = 1.0;"),
+    "topk_ties_to_higher_index": ("return (x->i < y->i) ? -1 : (x->i > y->i);",
+                                  "return (x->i > y->i) ? -1 : (x->i < y->i);"),
+    "topk_ascending": ("if (x->s > y->s) return -1;\n    if (x->s < y->s) return 1;",
+                       "if (x->s < y->s) return -1;\n    if (x->s > y->s) return 1;"),
+    "softmax_not_normalised": ("double w = exp(score[j] - m) / Z;", "double w = exp(score[j] - m);"),
+    "value_row_by_position": ("const uint16_t *row = v + (int64_t)idx[j] * ld;",
+                              "const uint16_t *row = v + (int64_t)j * ld;"),
+    "window_off_by_one": ("int lo = L - W > 0 ? L - W : 0;", "int lo = L - W + 1 > 0 ? L - W + 1 : 0;"),
+    "cosine_without_norms": ("? dot_bf(q, cached[c], d) / sqrt(nq * nc)", "? dot_bf(q, cached[c], d)"),
+    "fallback_non_strict": ("(rho_max[h] < tau ||", "(rho_max[h] <= tau ||"),
+    "t_dec_from_zero": ("int t_dec = seq[2] + 1;", "int t_dec = seq[2];"),
+    "fifo_head_not_advanced": ("seq[0] = (head + 1) % C;", "seq[0] = head;"),
+    "no_dedup": ("if (M == 0 || all[j] != out[M - 1])", "if (1)"),
+    "init_not_causal": ("flen[h * C + c] = oracle_exact_one(qq, kb, NULL, d, p + 1,",
+                        "flen[h * C + c] = oracle_exact_one(qq, kb, NULL, d, L0,"),
+    "gqa_interleaved": ("const uint16_t *kb = k + (int64_t)(h / G) * max_len * d;\n        const uint16_t *vb",
+                        "const uint16_t *kb = k + (int64_t)(h % Hkv) * max_len * d;\n        const uint16_t *vb"),
+    "recall_ties_to_newer": ("        p[c].i = c;\n    }\n    qsort(p, (size_t)n, sizeof(pair_t), cmp_pair);",
+                             "        p[c].i = n - 1 - c;\n    }\n    qsort(p, (size_t)n, sizeof(pair_t), cmp_pair);\n"
+                             "    for (int c = 0; c < n; ++c) p[c].i = n - 1 - p[c].i;"),
+    "reuse_ignores_window": ("    total += L - lo;", "    total += 0; lo = L;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    src = open(SRC).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    mut = tmp_path / "mut.c"
+    mut.write_text(src.replace(old, new))
+    so = tmp_path / "libmut.so"
+    subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+                           "-ffp-contract=off", str(mut), "-o", str(so), "-lm"])
+    lib = oracle.load(str(so))
+    caught = []
+    for pin in P.ALL_PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            caught.append(pin.__name__)
+    del lib
+    assert caught, f"mutant {name} passed every pin"
