@@ -1,0 +1,200 @@
+/*
+ * retopk.h -- C ABI of the GB300 (sm_103a) decode-time Top-K sparse attention
+ * library: ReTopK similarity-guided support reuse and the Exact Top-K path it
+ * falls back to.
+ *
+ * Method: "Recall Before You Rank: Similarity-Guided Top-K Reuse for Efficient
+ * Long-Context Attention" (ReTopK), §Methodology.  Each entry point names the
+ * equations it executes.
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are raw device pointers owned by the caller.  bf16 tensors are
+ *     passed as retopk_bf16 (the IEEE bfloat16 bit pattern).  Every tensor must
+ *     be 16-byte aligned and contiguous in the layout stated for it.
+ *   - head_dim d must be 128.  Query head h reads KV head h / (Hq / Hkv)
+ *     (consecutive GQA groups).
+ *   - K cache / V cache layout: [B, Hkv, max_len, d] bf16, row-major.  Row i of
+ *     (b, h_kv) is the key (value) of token i, 0-based.
+ *   - seqlens: device int32 [B].  seqlens[b] = L_b, the number of valid rows of
+ *     sequence b, INCLUDING the token being decoded (its key and value are in
+ *     the cache before the step runs).
+ *   - `stream` is a cudaStream_t.  Every call is asynchronous on it, never
+ *     synchronises the device (except where stated: create, init, export,
+ *     import, status and counter reads) and never allocates device memory:
+ *     the caller provides the workspace.
+ *   - Return value: RETOPK_OK (0) or a negative RETOPK_ERR_* code.  Argument
+ *     errors are detected on the host before anything is launched.  Faults the
+ *     device detects (an out-of-range support index in the cache, a full KV
+ *     cache on append) set bits in a sticky status word (retopk_get_status);
+ *     no kernel traps or asserts.
+ *   - Top-K ties are broken towards the lower key index; when fewer than K
+ *     keys (or candidates) exist, the support is all of them.
+ */
+#ifndef RETOPK_H
+#define RETOPK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t retopk_bf16;           /* raw bfloat16 bits */
+typedef struct retopk_ctx retopk_ctx;   /* opaque, host-side */
+
+enum {
+    RETOPK_OK = 0,
+    RETOPK_ERR_INVALID = -1,      /* bad pointer, size or hyper-parameter           */
+    RETOPK_ERR_UNSUPPORTED = -2,  /* head_dim != 128, group too large, length too big */
+    RETOPK_ERR_WORKSPACE = -3,    /* workspace too small or misaligned              */
+    RETOPK_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed           */
+    RETOPK_ERR_ALIGN = -5,        /* a tensor pointer is not 16-byte aligned        */
+    RETOPK_ERR_STATE = -6         /* state buffer of the wrong size or version      */
+};
+
+/* Status bits (sticky, set by device code). */
+#define RETOPK_STATUS_BAD_INDEX   0x1u  /* cached support index outside [0, L)      */
+#define RETOPK_STATUS_KV_FULL     0x2u  /* append with seqlens[b] == max_len        */
+#define RETOPK_STATUS_NONFINITE   0x4u  /* a non-finite score was produced          */
+
+/* Path codes reported per (sequence, query head), Eq. (13). */
+#define RETOPK_PATH_REUSE    0
+#define RETOPK_PATH_FALLBACK 1          /* rho_max < tau                            */
+#define RETOPK_PATH_REFRESH  2          /* T_r > 0 and t_dec a multiple of T_r       */
+
+/* ReTopK hyper-parameters (§Reliable Reuse, §Implementation settings):
+ * K support size, C cache capacity, W recent window, R retrieved entries,
+ * T_r refresh period (0 disables refresh), tau similarity threshold.
+ * Limits: d = 128; 1 <= Hq/Hkv <= 32; 1 <= K <= 4096; 1 <= R <= C <= 256;
+ * 0 <= W; max_len <= 2^20 (the candidate bitmap lives in shared memory). */
+typedef struct retopk_config {
+    int32_t batch;        /* B                                                  */
+    int32_t n_q_heads;    /* Hq                                                 */
+    int32_t n_kv_heads;   /* Hkv, divides Hq                                    */
+    int32_t head_dim;     /* d, must be 128                                     */
+    int32_t max_len;      /* rows per (b, h_kv) in the caller's KV cache        */
+    int32_t K, C, W, R, T_r;
+    float tau;
+} retopk_config;
+
+/* ---- context ------------------------------------------------------------ */
+
+/* Bytes of device workspace a context with this configuration needs.
+ * Returns 0 if the configuration is invalid. */
+size_t retopk_workspace_bytes(const retopk_config *cfg);
+
+/* Creates a context that keeps all its state (the per-head query-support
+ * cache of Eq. (5), decode counters, scratch) in the caller's device
+ * workspace `d_workspace` (>= retopk_workspace_bytes, 256-byte aligned).
+ * The context object itself is host memory owned by the library; free it
+ * with retopk_destroy.  Synchronises the current device once (clears the
+ * workspace).  The workspace must outlive the context. */
+int retopk_create(const retopk_config *cfg, void *d_workspace, size_t bytes, retopk_ctx **out);
+int retopk_destroy(retopk_ctx *ctx);
+
+/* ---- ReTopK decode ------------------------------------------------------ */
+
+/* Cache initialisation from the final C prompt tokens (§Recall-Before-Rerank,
+ * "query-support cache"): for prompt position p = L0_b - C + c, c = 0..C-1,
+ * stores the query and its Exact Top-K support over the causal prefix
+ * 0..p (Eq. (1)).  q_last: [B, Hq, C, d] bf16, the queries of positions
+ * L0-C .. L0-1.  d_prompt_len: device int32 [B] = L0_b (each >= C).
+ * Resets the decode counter t_dec to 0.  Synchronises `stream` once to read
+ * the prompt lengths (set-up, not part of the decode step). */
+int retopk_init_cache(retopk_ctx *ctx, const retopk_bf16 *q_last, const retopk_bf16 *k_cache,
+                      const int32_t *d_prompt_len, void *stream);
+
+/* Appends one token per sequence: writes k_new / v_new ([B, Hkv, d]) into
+ * row seqlens[b] of the caches and increments seqlens[b] on the device.
+ * A full cache (seqlens[b] == max_len) sets RETOPK_STATUS_KV_FULL and leaves
+ * that sequence unchanged.  Graph-capturable. */
+int retopk_append_kv(retopk_ctx *ctx, const retopk_bf16 *k_new, const retopk_bf16 *v_new,
+                     retopk_bf16 *k_cache, retopk_bf16 *v_cache, int32_t *d_seqlens,
+                     void *stream);
+
+/* One ReTopK decode step for every (sequence, query head):
+ *   Eq. (6)-(7)  cosine recall of q against the head's cached queries, Top-R
+ *   Eq. (13)     path: refresh / similarity fallback / reuse (decided on device)
+ *   reuse:       Eq. (8)-(9) candidates = retrieved supports U recent window,
+ *                Eq. (10) exact rerank scores of the candidates only,
+ *                Eq. (11) Top-K of the candidates
+ *   exact:       Eq. (4) full-history scores, Eq. (1) global Top-K
+ *   both:        Eq. (12) softmax-value aggregation over the support, then the
+ *                cache insertion of (q, support) and t_dec += 1.
+ * q: [B, Hq, d] bf16; out: [B, Hq, d] bf16.  No host round trip: the path
+ * switch lives on the device, so the call can be captured in a CUDA graph. */
+int retopk_decode_step(retopk_ctx *ctx, const retopk_bf16 *q, const retopk_bf16 *k_cache,
+                       const retopk_bf16 *v_cache, const int32_t *d_seqlens,
+                       retopk_bf16 *out, void *stream);
+
+/* Per-step diagnostics of the last decode step, copied to HOST buffers
+ * (synchronises `stream`).  Any pointer may be NULL.
+ *   path     [B*Hq] int32   RETOPK_PATH_*
+ *   rho_max  [B*Hq] float   max cosine (-inf for an empty cache)
+ *   topR     [B*Hq*R] int32 retrieved entries as logical positions
+ *                           (0 = oldest live entry), -1 padded
+ *   M        [B*Hq] int32   |A_t| on reuse heads, L on exact heads
+ *   cand     [B*Hq*(R*K+W)] int32  A_t ascending on reuse heads, -1 padded
+ *   support  [B*Hq*K] int32 the selected support ascending, -1 padded
+ *   sup_len  [B*Hq] int32
+ *   out_f32  [B*Hq*d] float the step output before bf16 rounding */
+int retopk_get_diagnostics(retopk_ctx *ctx, int32_t *path, float *rho_max, int32_t *topR,
+                           int32_t *M, int32_t *cand, int32_t *support, int32_t *sup_len,
+                           float *out_f32, void *stream);
+
+/* Path counters since create/init (host buffers, synchronises):
+ * counts[0..2] = steps x heads on reuse / fallback / refresh,
+ * counts[3] = sum of M_t over reuse head-steps, counts[4] = max M_t. */
+int retopk_get_counters(retopk_ctx *ctx, int64_t counts[5], void *stream);
+
+/* Cache state export / import (checkpoint, and state-forced testing).
+ * Host buffer layout, little-endian, contiguous:
+ *   fifo_q   [B, Hq, C, d]  uint16 (raw bf16 query bits)
+ *   fifo_sup [B, Hq, C, K]  int32  (ascending support, -1 padded)
+ *   fifo_len [B, Hq, C]     int32
+ *   seq      [B, 3]         int32  (next slot, live count, t_dec)
+ * Live entry c (0 = oldest) of sequence b sits in slot
+ * (seq[b][0] - seq[b][1] + c) mod C.  Both calls synchronise `stream`. */
+size_t retopk_state_bytes(const retopk_ctx *ctx);
+int retopk_export_state(retopk_ctx *ctx, void *host_buf, size_t bytes, void *stream);
+int retopk_import_state(retopk_ctx *ctx, const void *host_buf, size_t bytes, void *stream);
+
+/* Sticky device status word (RETOPK_STATUS_* bits); `clear` resets it.
+ * Synchronises `stream`. */
+int retopk_get_status(retopk_ctx *ctx, uint32_t *bits, int clear, void *stream);
+
+const char *retopk_strerror(int code);
+
+/* ---- Exact Top-K (stateless) -------------------------------------------- */
+
+/* Device workspace for exact_topk_attention_step with these sizes
+ * (0 if invalid). */
+size_t exact_topk_workspace_bytes(int B, int Hq, int Hkv, int d, int max_len, int K);
+
+/* Exact Top-K attention (§Motivation Eq. (1), §Problem Setup Eq. (4),
+ * §Recall-Before-Rerank Eq. (12)): for every (b, h) scores all L_b keys,
+ * selects the K best (ties to the lower index) and aggregates their values
+ * with softmax weights.  q: [B, Hq, d]; out: [B, Hq, d] bf16.
+ * idx_out: optional device int32 [B, Hq, K], the support ascending, -1
+ * padded when L_b < K.  d_workspace: >= exact_topk_workspace_bytes,
+ * 256-byte aligned.  Graph-capturable. */
+int exact_topk_attention_step(const retopk_bf16 *q, const retopk_bf16 *k_cache,
+                              const retopk_bf16 *v_cache, const int32_t *d_seqlens,
+                              int B, int Hq, int Hkv, int d, int max_len, int K,
+                              retopk_bf16 *out, int32_t *idx_out,
+                              void *d_workspace, size_t bytes, void *stream);
+
+/* ---- profiling ----------------------------------------------------------- */
+
+/* Optional per-kernel timing: when enabled, every launch records CUDA events
+ * around the full-history scan kernel on its stream; retopk_profile_read
+ * returns the number of scan launches and their summed duration in ms since
+ * the last read (synchronises).  Off by default; not for use during capture. */
+int retopk_profile_enable(int on);
+int retopk_profile_read(int64_t *scan_launches, double *scan_ms);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RETOPK_H */

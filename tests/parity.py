@@ -1,0 +1,178 @@
+"""GPU-vs-oracle comparison helpers (used by the -m gpu tests and smoke()).
+
+Tolerances (written here, applied everywhere):
+  * path decisions: identical unless the oracle's |rho_max - tau| < 1e-4;
+  * retrieved entries R_t: the same set unless the oracle's R-th and (R+1)-th
+    cosines are within 1e-4 of each other;
+  * candidate sets A_t (when path and R_t agree): identical;
+  * supports: identical up to swaps among keys whose oracle score lies within
+    1e-3 of the oracle's K-th score;
+  * outputs: max-abs <= 2e-2 and relative L2 <= 1e-2 against the oracle's
+    fp64 Eq. (12) output on the GPU's own support (and, where the supports
+    agree, against the oracle's output).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+
+TAU_BAND = 1e-4
+RHO_TOL = 1e-5
+SCORE_BAND = 1e-3
+OUT_MAX_ABS = 2e-2
+OUT_REL_L2 = 1e-2
+
+
+def bf16_to_f32(h: np.ndarray) -> np.ndarray:
+    return (np.ascontiguousarray(h).astype(np.uint32) << 16).view(np.float32)
+
+
+def out_close(got: np.ndarray, ref: np.ndarray):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    mx = float(np.abs(got - ref).max()) if got.size else 0.0
+    rel = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
+    return (mx <= OUT_MAX_ABS and rel <= OUT_REL_L2), mx, rel
+
+
+def support_ok(q, k_rows, got, want, kth):
+    """Supports may differ only among keys scoring within SCORE_BAND of the K-th."""
+    got = [int(x) for x in got]
+    want = [int(x) for x in want]
+    if len(got) != len(want):
+        return False, f"support length {len(got)} != {len(want)}"
+    if len(set(got)) != len(got):
+        return False, "duplicate index in support"
+    if got != sorted(got):
+        return False, "support not ascending"
+    diff = sorted(set(got) ^ set(want))
+    if not diff:
+        return True, ""
+    s = oracle.scores(q, k_rows, np.array(diff, dtype=np.int32))
+    bad = [(i, float(x)) for i, x in zip(diff, s) if abs(x - kth) > SCORE_BAND]
+    if bad:
+        return False, f"{len(diff)} differing keys, {len(bad)} outside the band, e.g. {bad[:4]} (kth={kth})"
+    return True, f"{len(diff)} near-tie swaps"
+
+
+def compare_exact(q, k, v, L, K, gpu_idx, gpu_out, where=""):
+    """Exact Top-K: q [B,Hq,d], k/v [B,Hkv,T,d] bits, L [B]; gpu_idx [B,Hq,K] (-1 pad); gpu_out [B,Hq,d] f32."""
+    B, Hq, d = q.shape
+    G = Hq // k.shape[1]
+    sup, sup_len, kth, out = oracle.exact_step(q, k, v, L, K)
+    errs = []
+    for b in range(B):
+        for h in range(Hq):
+            n = int(sup_len[b, h])
+            g = gpu_idx[b, h]
+            gs = g[g >= 0]
+            if (g[len(gs):] != -1).any() or not (g[:len(gs)] >= 0).all():
+                errs.append(f"{where} b{b} h{h}: bad -1 padding")
+                continue
+            kr = k[b, h // G]
+            ok, msg = support_ok(q[b, h], kr, gs, sup[b, h, :n], kth[b, h])
+            if not ok:
+                errs.append(f"{where} b{b} h{h}: {msg}")
+                continue
+            ref = oracle.attention_on_support(q[b, h], kr, v[b, h // G], gs)
+            ok, mx, rel = out_close(gpu_out[b, h], ref)
+            if not ok:
+                errs.append(f"{where} b{b} h{h}: out max {mx:.3g} rel {rel:.3g}")
+            ok, mx, rel = out_close(gpu_out[b, h], out[b, h])
+            if not ok:
+                errs.append(f"{where} b{b} h{h}: out vs oracle support max {mx:.3g} rel {rel:.3g}")
+    return errs
+
+
+def oracle_state_from_gpu(st: dict, b: int, K: int) -> oracle.CacheState:
+    Hq, C, d = st["fifo_q"].shape[1], st["fifo_q"].shape[2], st["fifo_q"].shape[3]
+    cs = oracle.CacheState(Hq, C, K, d)
+    cs.fq[...] = st["fifo_q"][b]
+    cs.fsup[...] = st["fifo_sup"][b]
+    cs.flen[...] = st["fifo_len"][b]
+    cs.seq[...] = st["seq"][b]
+    return cs
+
+
+def compare_decode_step(pre: dict, post: dict, diag: dict, q_t, k, v, L, w, gpu_out_bf16, where=""):
+    """State-forced check of one decode step for every sequence.
+
+    pre / post: the GPU's exported cache state before / after the step.
+    q_t [B,Hq,d] bits; k, v [B,Hkv,T,d] bits; L [B] (current token included).
+    Returns (errors, stats).
+    """
+    B, Hq, d = q_t.shape
+    G = Hq // w.Hkv
+    R, K, C = w.R, w.K, w.C
+    errs = []
+    stats = dict(path_band=0, topR_band=0, swaps=0, heads=0)
+    for b in range(B):
+        cs = oracle_state_from_gpu(pre, b, K)
+        r = oracle.decode_step(cs, q_t[b], k[b], v[b], int(L[b]), w.Hkv, w.W, R, w.T_r, w.tau)
+        for h in range(Hq):
+            bh = b * Hq + h
+            stats["heads"] += 1
+            tag = f"{where} b{b} h{h}"
+            po, pg = int(r["path"][h]), int(diag["path"][bh])
+            rmax_o, rmax_g = float(r["rho_max"][h]), float(diag["rho_max"][bh])
+            if np.isfinite(rmax_o) or np.isfinite(rmax_g):
+                if abs(rmax_o - rmax_g) > RHO_TOL:
+                    errs.append(f"{tag}: rho_max {rmax_g} vs oracle {rmax_o}")
+            if po != pg:
+                if po != 2 and pg != 2 and abs(rmax_o - w.tau) < TAU_BAND:
+                    stats["path_band"] += 1
+                    continue
+                errs.append(f"{tag}: path {pg} vs oracle {po} (rho_max {rmax_o})")
+                continue
+            kr, vr = k[b, h // G], v[b, h // G]
+            # retrieved entries (as a set)
+            count = int(pre["seq"][b, 1])
+            nr = min(R, count)
+            to, tg = set(r["topR"][h, :nr].tolist()), set(diag["topR"][bh, :nr].tolist())
+            topR_same = to == tg
+            if not topR_same:
+                rho = np.sort(r["rho"][h, :count])[::-1]
+                if nr < count and abs(rho[nr - 1] - rho[nr]) < TAU_BAND:
+                    stats["topR_band"] += 1
+                else:
+                    errs.append(f"{tag}: topR {sorted(tg)} vs oracle {sorted(to)}")
+                    continue
+            if po == 0 and topR_same:
+                Mo, Mg = int(r["M"][h]), int(diag["M"][bh])
+                if Mo != Mg or not np.array_equal(r["cand"][h, :Mo], diag["cand"][bh, :Mg]):
+                    errs.append(f"{tag}: candidate set differs (M {Mg} vs {Mo})")
+                    continue
+            gs = diag["support"][bh, :int(diag["sup_len"][bh])]
+            if po == 0 and not topR_same:
+                # different (legal) retrieval: check the GPU's own support against
+                # the rerank of its own candidate set
+                A = diag["cand"][bh, :int(diag["M"][bh])]
+                e = oracle.scores(q_t[b, h], kr, A)
+                want = np.sort(oracle.topk(e, K, idx=A))
+                kth = float(np.sort(e)[::-1][min(K, len(e)) - 1]) if len(e) else 0.0
+            else:
+                want = r["sup"][h, :int(r["sup_len"][h])]
+                kth = float(r["kth"][h])
+            ok, msg = support_ok(q_t[b, h], kr, gs, want, kth)
+            if not ok:
+                errs.append(f"{tag}: support {msg}")
+                continue
+            if msg:
+                stats["swaps"] += 1
+            ref = oracle.attention_on_support(q_t[b, h], kr, vr, gs)
+            ok1, mx, rel = out_close(bf16_to_f32(gpu_out_bf16[b, h]), ref)
+            ok2, mx2, rel2 = out_close(diag["out_f32"][bh], ref)
+            if not (ok1 and ok2):
+                errs.append(f"{tag}: out max {mx:.3g}/{mx2:.3g} rel {rel:.3g}/{rel2:.3g}")
+            # the cache slot written by this step
+            slot = int(pre["seq"][b, 0])
+            if not np.array_equal(post["fifo_q"][b, h, slot], q_t[b, h]):
+                errs.append(f"{tag}: cached query bits differ")
+            n = int(post["fifo_len"][b, h, slot])
+            if n != len(gs) or not np.array_equal(post["fifo_sup"][b, h, slot, :n], gs):
+                errs.append(f"{tag}: cached support differs from the step's support")
+        exp_seq = [(int(pre["seq"][b, 0]) + 1) % C, min(int(pre["seq"][b, 1]) + 1, C), int(pre["seq"][b, 2]) + 1]
+        if post["seq"][b].tolist() != exp_seq:
+            errs.append(f"{where} b{b}: seq {post['seq'][b].tolist()} vs {exp_seq}")
+    return errs, stats

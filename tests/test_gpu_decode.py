@@ -1,0 +1,248 @@
+"""ReTopK decode steps through the C ABI against the fp64 oracle (GPU).
+
+State-forced protocol: before a checked step the GPU's cache state is
+exported and handed to the oracle, which computes the same step from that
+state; path, rho_max, retrieved entries, candidate set, support, output and
+the cache slot written are then compared (tolerances in tests/parity.py).
+This keeps one legal near-tie swap from turning every later step into a
+mismatch.  Unchecked steps still run on the GPU, so the state being checked
+is the GPU's own trajectory.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import compare_decode_step, out_close
+from top_sparse_attention_exact_gb300 import synth
+from top_sparse_attention_exact_gb300.runner import DecodeRun, ExactRun
+
+pytestmark = pytest.mark.gpu
+
+
+def run_checked(w, check_steps=None, arrays=None, max_len=None):
+    dr = DecodeRun(w, arrays=arrays, max_len=max_len)
+    k, v, qd = dr.k_host, dr.v_host, dr.qd_host
+    errs, agg = [], dict(path_band=0, topR_band=0, swaps=0, heads=0)
+    paths = []
+    for t in range(w.steps):
+        check = check_steps is None or (t + 1) in check_steps
+        if check:
+            pre = dr.ctx.retopk_export_state()
+        dr.step(t)
+        if check:
+            torch.cuda.synchronize()
+            post = dr.ctx.retopk_export_state()
+            diag = dr.ctx.retopk_get_diagnostics()
+            paths.append(diag["path"].copy())
+            L = dr.seqlens.cpu().numpy()
+            out = dr.out.cpu().numpy().view(np.uint16)
+            e, st = compare_decode_step(pre, post, diag, qd[t], k, v, L, w, out, where=f"{w.name} t{t + 1}")
+            errs += e
+            for key in agg:
+                agg[key] += st[key]
+    assert dr.ctx.retopk_get_status() == 0
+    return dr, errs, agg, paths
+
+
+def test_tiny_full_trajectory():
+    w = synth.WORKLOADS["tiny_1h_2k"]
+    dr, errs, agg, paths = run_checked(w)
+    assert not errs, "\n".join(errs[:20])
+    p = np.concatenate(paths)
+    # refresh exactly at t_dec = 16, 32, 48, 64
+    assert [i + 1 for i, x in enumerate(p) if x == 2] == [16, 32, 48, 64]
+    assert (p == 0).sum() > 0 and (p == 1).sum() > 0
+
+
+def test_tiny_free_running_matches_oracle():
+    """Both sides run their own trajectory; on this case no near-ties occur."""
+    w = synth.WORKLOADS["tiny_1h_2k"]
+    dr = DecodeRun(w)
+    k, v, qp, qd = dr.k_host, dr.v_host, dr.qp_host, dr.qd_host
+    st = oracle.init_cache(qp[0], k[0], w.L0, w.Hq, w.Hkv, w.K, w.C)
+    g0 = dr.ctx.retopk_export_state()
+    assert np.array_equal(g0["fifo_len"][0], st.flen)
+    for h in range(w.Hq):
+        for c in range(w.C):
+            n = st.flen[h, c]
+            assert np.array_equal(g0["fifo_sup"][0, h, c, :n], st.fsup[h, c, :n])
+    for t in range(w.steps):
+        dr.step(t)
+        r = oracle.decode_step(st, qd[t, 0], k[0], v[0], w.L0 + t + 1, w.Hkv, w.W, w.R, w.T_r, w.tau)
+        diag = dr.ctx.retopk_get_diagnostics()
+        assert diag["path"].tolist() == r["path"].tolist(), t
+        assert diag["support"][0, :diag["sup_len"][0]].tolist() == r["sup"][0, :r["sup_len"][0]].tolist(), t
+        ok, mx, rel = out_close(diag["out_f32"][0], r["out"][0])
+        assert ok, (t, mx, rel)
+    g = dr.ctx.retopk_export_state()
+    assert g["seq"][0].tolist() == st.seq.tolist()
+    assert np.array_equal(g["fifo_q"][0], st.fq)
+
+
+def test_init_cache_matches_oracle_qwen_shape():
+    w = synth.scaled(synth.WORKLOADS["qwen7b_16k"], steps=1)
+    dr = DecodeRun(w)
+    g = dr.ctx.retopk_export_state()
+    st = oracle.init_cache(dr.qp_host[0], dr.k_host[0], w.L0, w.Hq, w.Hkv, w.K, w.C)
+    assert g["seq"][0].tolist() == [0, w.C, 0]
+    assert np.array_equal(g["fifo_q"][0], st.fq)
+    from parity import support_ok
+    for h in range(w.Hq):
+        for c in range(w.C):
+            n = st.flen[h, c]
+            p = w.L0 - w.C + c
+            kr = dr.k_host[0, h // 7]
+            got = g["fifo_sup"][0, h, c, :g["fifo_len"][0, h, c]]
+            if not np.array_equal(got, st.fsup[h, c, :n]):
+                s = oracle.scores(dr.qp_host[0, h, c], kr[:p + 1])
+                kth = np.sort(s)[::-1][n - 1]
+                ok, msg = support_ok(dr.qp_host[0, h, c], kr, got, st.fsup[h, c, :n], kth)
+                assert ok, (h, c, msg)
+
+
+def test_qwen_16k_all_steps():
+    w = synth.WORKLOADS["qwen7b_16k"]
+    dr, errs, agg, paths = run_checked(w)
+    assert not errs, "\n".join(errs[:20])
+    c = dr.ctx.retopk_get_counters()
+    assert c["reuse"] + c["fallback"] + c["refresh"] == w.steps * w.Hq
+    assert c["refresh"] == (w.steps // w.T_r) * w.Hq
+    assert c["max_M"] <= w.R * w.K + w.W
+
+
+@pytest.mark.parametrize("name", ["qwen7b_32k", "qwen7b_64k"])
+def test_qwen_longer_sampled(name):
+    w = synth.WORKLOADS[name]
+    steps = set(range(1, 9)) | set(range(125, 133)) | {200, 255, 256}
+    dr, errs, agg, paths = run_checked(w, check_steps=steps)
+    assert not errs, "\n".join(errs[:20])
+
+
+def test_headline_128k_sampled():
+    w = synth.WORKLOADS["qwen7b_128k"]
+    steps = {1, 2, 3, 64, 127, 128, 129, 256, 384, 511, 512}
+    dr, errs, agg, paths = run_checked(w, check_steps=steps)
+    assert not errs, "\n".join(errs[:20])
+
+
+@pytest.fixture(scope="module")
+def sweep_arrays():
+    w = synth.batched_sweep(256, 0.70, steps=24)
+    return w, synth.generate(w)
+
+
+@pytest.mark.parametrize("K", [256, 1024, 2048])
+@pytest.mark.parametrize("tau", [0.70, 0.95])
+def test_batched_sweep_sampled(sweep_arrays, K, tau):
+    w0, arrays = sweep_arrays
+    w = synth.scaled(w0, K=K, tau=tau, name=f"sweep_K{K}_tau{tau}")
+    dr, errs, agg, paths = run_checked(w, check_steps={1, 2, 12, 24}, arrays=arrays)
+    assert not errs, "\n".join(errs[:20])
+
+
+def _degenerate(tau, T_r, W, steps=12):
+    w = synth.scaled(synth.WORKLOADS["qwen7b_16k"], L0=3000, steps=steps, tau=tau, T_r=T_r, W=W,
+                     name=f"deg_tau{tau}_Tr{T_r}_W{W}")
+    return w
+
+
+def test_tau_above_one_equals_exact_every_step():
+    w = _degenerate(1.5, 0, 32)
+    dr = DecodeRun(w)
+    ex = ExactRun(dr)
+    for t in range(w.steps):
+        dr.step(t)
+        diag = dr.ctx.retopk_get_diagnostics()
+        assert (diag["path"] == 1).all()
+        ex.step(dr.q_dec[t])
+        torch.cuda.synchronize()
+        assert torch.equal(ex.out, dr.out)
+        assert np.array_equal(ex.idx.view(-1, w.K).cpu().numpy(), diag["support"])
+
+
+def test_window_covering_history_equals_exact():
+    w = _degenerate(-2.0, 0, 100000)
+    dr = DecodeRun(w)
+    ex = ExactRun(dr)
+    for t in range(w.steps):
+        dr.step(t)
+        diag = dr.ctx.retopk_get_diagnostics()
+        assert (diag["path"] == 0).all()
+        assert (diag["M"] == w.L0 + t + 1).all()
+        ex.step(dr.q_dec[t])
+        torch.cuda.synchronize()
+        # the rerank scores (CUDA cores) and the scan scores (tensor cores) may
+        # round differently, so near-ties may swap; outputs agree to tolerance
+        from parity import support_ok
+        L = w.L0 + t + 1
+        eidx = ex.idx.view(-1, w.K).cpu().numpy()
+        for h in range(w.Hq):
+            kr = dr.k_host[0, h // 7]
+            s = oracle.scores(dr.qd_host[t, 0, h], kr[:L])
+            kth = float(np.sort(s)[::-1][w.K - 1])
+            ok, msg = support_ok(dr.qd_host[t, 0, h], kr, diag["support"][h], eidx[h], kth)
+            assert ok, (t, h, msg)
+        a = synth.bf16_bits_to_f32(ex.out.cpu().numpy().view(np.uint16))
+        b = synth.bf16_bits_to_f32(dr.out.cpu().numpy().view(np.uint16))
+        ok, mx, rel = out_close(a, b)
+        assert ok, (t, mx, rel)
+
+
+def test_refresh_every_step_and_always_reuse():
+    dr = DecodeRun(_degenerate(0.85, 1, 32))
+    for t in range(dr.w.steps):
+        dr.step(t)
+        assert (dr.ctx.retopk_get_diagnostics()["path"] == 2).all()
+    dr = DecodeRun(_degenerate(-1.0, 0, 32))
+    for t in range(dr.w.steps):
+        dr.step(t)
+        assert (dr.ctx.retopk_get_diagnostics()["path"] == 0).all()
+
+
+def test_graph_replay_matches_eager():
+    w = synth.scaled(synth.WORKLOADS["qwen7b_16k"], steps=40, T_r=16)
+    a = DecodeRun(w)
+    b = DecodeRun(w, arrays=(a.k_host, a.v_host, a.qp_host, a.qd_host))
+    b.capture()
+    for t in range(w.steps):
+        a.step(t)
+        b.replay(t)
+        torch.cuda.synchronize()
+        assert torch.equal(a.out, b.out), t
+    sa, sb = a.ctx.retopk_export_state(), b.ctx.retopk_export_state()
+    for key in sa:
+        assert np.array_equal(sa[key], sb[key]), key
+    assert torch.equal(a.seqlens, b.seqlens)
+
+
+def test_state_round_trip_and_status_bits():
+    w = synth.scaled(synth.WORKLOADS["qwen7b_16k"], L0=2048, steps=4)
+    dr = DecodeRun(w)
+    dr.step(0)
+    st = dr.ctx.retopk_export_state()
+    dr.ctx.retopk_import_state(st)
+    st2 = dr.ctx.retopk_export_state()
+    for key in st:
+        assert np.array_equal(st[key], st2[key])
+    # a support index beyond the history is reported, not followed
+    bad = {k: v.copy() for k, v in st.items()}
+    bad["fifo_sup"][0, :, :, 0] = 10 ** 6
+    dr.ctx.retopk_import_state(bad)
+    dr.ctx.retopk_decode_step(dr.q_dec[1], dr.k_cache, dr.v_cache, dr.seqlens, dr.out)
+    s = dr.ctx.retopk_get_status(clear=True)
+    diag = dr.ctx.retopk_get_diagnostics()
+    if (diag["path"] == 0).any():
+        assert s & 0x1
+    assert dr.ctx.retopk_get_status() == 0
+    # appending to a full cache is reported and leaves the length unchanged
+    dr.seqlens.fill_(dr.max_len)
+    dr.ctx.retopk_append_kv(dr.k_new[0], dr.v_new[0], dr.k_cache, dr.v_cache, dr.seqlens)
+    assert dr.ctx.retopk_get_status() & 0x2
+    assert (dr.seqlens.cpu() == dr.max_len).all()
+    # malformed state buffers are refused on the host
+    bad = {k: v.copy() for k, v in st.items()}
+    bad["seq"][0, 0] = w.C
+    from top_sparse_attention_exact_gb300.retopk import RetopkError
+    with pytest.raises(RetopkError):
+        dr.ctx.retopk_import_state(bad)

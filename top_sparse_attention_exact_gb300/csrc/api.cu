@@ -1,0 +1,591 @@
+// api.cu -- the C ABI declared in include/retopk.h: argument checking,
+// workspace layout and the launch sequence of each entry point.  No device
+// memory is allocated here; every buffer lives in the caller's workspace.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+
+namespace retopk {
+cudaError_t configure_scan();
+cudaError_t configure_select();
+cudaError_t configure_recall(int bytes);
+}  // namespace retopk
+
+using namespace retopk;
+
+struct retopk_ctx {
+    retopk_config cfg;
+    Work w;
+    void *ws;
+    size_t ws_bytes;
+    int device;
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+struct Layout {
+    size_t off[32];
+    int n = 0;
+    size_t total = 0;
+    size_t add(size_t bytes)
+    {
+        total = (total + kAlign - 1) / kAlign * kAlign;
+        const size_t o = total;
+        total += bytes;
+        off[n++] = o;
+        return o;
+    }
+};
+
+int sm_count()
+{
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+            n = 1;
+    }
+    return n;
+}
+
+int ensure_configured()
+{
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = configure_scan();
+        if (err == cudaSuccess)
+            err = configure_select();
+        if (err == cudaSuccess)
+            err = configure_recall(kMaxLen / 8);
+    });
+    return err == cudaSuccess ? RETOPK_OK : RETOPK_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+int n_filter_for(int max_len) { return std::min(kMaxSeg, std::max(1, (max_len + 8191) / 8192)); }
+
+int cand_stride_for(int max_len, int n_filter, int RKW)
+{
+    const int seg = (((max_len + n_filter - 1) / n_filter) + 255) & ~255;
+    const int s = std::max(seg * n_filter, RKW);
+    return (s + 63) & ~63;
+}
+
+// Fills the sizes (and, when base != NULL, the pointers) of a workspace.
+size_t plan(const retopk_config &c, bool stateful, Work *w, char *base)
+{
+    Work x;
+    memset(&x, 0, sizeof x);
+    x.B = c.batch;
+    x.Hq = c.n_q_heads;
+    x.Hkv = c.n_kv_heads;
+    x.G = c.n_q_heads / c.n_kv_heads;
+    x.max_len = c.max_len;
+    x.K = c.K;
+    x.C = c.C;
+    x.W = c.W;
+    x.R = c.R;
+    x.T_r = c.T_r;
+    x.tau = c.tau;
+    x.n_filter = n_filter_for(c.max_len);
+    const int RKW = stateful ? c.R * c.K + c.W : 0;
+    x.cand_stride = cand_stride_for(c.max_len, x.n_filter, RKW);
+    x.n_rerank = stateful ? std::min(32, std::max(1, (RKW + 255) / 256)) : 1;
+    const size_t BH = (size_t)c.batch * c.n_q_heads;
+    Layout L;
+    size_t o_fq = 0, o_fs = 0, o_fl = 0, o_seq = 0, o_cnt = 0, o_path = 0, o_rho = 0, o_topr = 0;
+    if (stateful) {
+        o_fq = L.add(BH * c.C * kD * 2);
+        o_fs = L.add(BH * c.C * c.K * 4);
+        o_fl = L.add(BH * c.C * 4);
+        o_seq = L.add((size_t)c.batch * SEQ_WORDS * 4);
+        o_cnt = L.add((size_t)c.batch * CNT_WORDS * 8);
+        o_path = L.add(BH * 4);
+        o_rho = L.add(BH * 4);
+        o_topr = L.add(BH * c.R * 4);
+    }
+    const size_t o_M = L.add(BH * 4);
+    const size_t o_ci = L.add(BH * x.cand_stride * 4);
+    const size_t o_ck = L.add(BH * x.cand_stride * 4);
+    const size_t o_sg = L.add(BH * x.n_filter * 4);
+    const size_t o_sc = L.add(BH * (size_t)c.max_len * 4);
+    const size_t o_h = L.add(BH * kHistBins * 4);
+    const size_t o_sup = L.add(BH * c.K * 4);
+    const size_t o_sl = L.add(BH * 4);
+    const size_t o_of = L.add(BH * kD * 4);
+    const size_t o_st = L.add(16);
+    if (base) {
+        if (stateful) {
+            x.fifo_q = (uint16_t *)(base + o_fq);
+            x.fifo_sup = (int32_t *)(base + o_fs);
+            x.fifo_len = (int32_t *)(base + o_fl);
+            x.seq = (int32_t *)(base + o_seq);
+            x.counters = (unsigned long long *)(base + o_cnt);
+            x.path = (int32_t *)(base + o_path);
+            x.rho_max = (float *)(base + o_rho);
+            x.topR = (int32_t *)(base + o_topr);
+        }
+        x.M = (int32_t *)(base + o_M);
+        x.cand_idx = (int32_t *)(base + o_ci);
+        x.cand_key = (uint32_t *)(base + o_ck);
+        x.seg_count = (int32_t *)(base + o_sg);
+        x.scores = (float *)(base + o_sc);
+        x.hist = (uint32_t *)(base + o_h);
+        x.support = (int32_t *)(base + o_sup);
+        x.sup_len = (int32_t *)(base + o_sl);
+        x.out_f32 = (float *)(base + o_of);
+        x.status = (uint32_t *)(base + o_st);
+    }
+    if (w)
+        *w = x;
+    return L.total + kAlign;
+}
+
+int check_dims(int B, int Hq, int Hkv, int d, int max_len, int K)
+{
+    if (B < 1 || Hq < 1 || Hkv < 1 || max_len < 1 || K < 1)
+        return RETOPK_ERR_INVALID;
+    if (Hq % Hkv != 0)
+        return RETOPK_ERR_INVALID;
+    if (d != kD || Hq / Hkv > kMaxGroup || max_len > kMaxLen || K > kMaxK)
+        return RETOPK_ERR_UNSUPPORTED;
+    return RETOPK_OK;
+}
+
+int check_cfg(const retopk_config *c)
+{
+    if (!c)
+        return RETOPK_ERR_INVALID;
+    int e = check_dims(c->batch, c->n_q_heads, c->n_kv_heads, c->head_dim, c->max_len, c->K);
+    if (e)
+        return e;
+    if (c->C < 1 || c->C > kMaxC || c->R < 1 || c->R > c->C || c->W < 0 || c->T_r < 0)
+        return RETOPK_ERR_INVALID;
+    if (isnan(c->tau))
+        return RETOPK_ERR_INVALID;
+    return RETOPK_OK;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? RETOPK_OK : RETOPK_ERR_CUDA; }
+
+// ---- optional scan timing -------------------------------------------------
+struct Prof {
+    std::mutex mu;
+    bool on = false;
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev;
+    long long done_launches = 0;
+    double done_ms = 0.0;
+} g_prof;
+
+void prof_begin(cudaStream_t st, cudaEvent_t *a)
+{
+    *a = nullptr;
+    if (!g_prof.on)
+        return;
+    if (cudaEventCreate(a) == cudaSuccess)
+        cudaEventRecord(*a, st);
+    else
+        *a = nullptr;
+}
+
+void prof_end(cudaStream_t st, cudaEvent_t a)
+{
+    if (!a)
+        return;
+    cudaEvent_t b;
+    if (cudaEventCreate(&b) != cudaSuccess) {
+        cudaEventDestroy(a);
+        return;
+    }
+    cudaEventRecord(b, st);
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    g_prof.ev.emplace_back(a, b);
+}
+
+int run_scan(const Work &w, QSrc q, const uint16_t *k, const int32_t *sl, int off, cudaStream_t st)
+{
+    cudaEvent_t ev;
+    prof_begin(st, &ev);
+    const cudaError_t e = launch_scan(w, q, k, sl, off, st);
+    prof_end(st, ev);
+    return cuda_rc(e);
+}
+
+int n_scan_for(int B, int Hkv, int max_len)
+{
+    const int target = sm_count() * scan_ctas_per_sm();
+    int n = (target + B * Hkv - 1) / (B * Hkv);
+    const int by_len = (max_len + 255) / 256;
+    return std::max(1, std::min(n, by_len));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t retopk_workspace_bytes(const retopk_config *cfg)
+{
+    if (check_cfg(cfg))
+        return 0;
+    return plan(*cfg, true, nullptr, nullptr);
+}
+
+int retopk_create(const retopk_config *cfg, void *d_workspace, size_t bytes, retopk_ctx **out)
+{
+    int e = check_cfg(cfg);
+    if (e)
+        return e;
+    if (!out || !d_workspace)
+        return RETOPK_ERR_INVALID;
+    if (((uintptr_t)d_workspace & (kAlign - 1)) != 0 || bytes < plan(*cfg, true, nullptr, nullptr))
+        return RETOPK_ERR_WORKSPACE;
+    if ((e = ensure_configured()))
+        return e;
+    retopk_ctx *c = (retopk_ctx *)calloc(1, sizeof(retopk_ctx));
+    if (!c)
+        return RETOPK_ERR_INVALID;
+    c->cfg = *cfg;
+    c->ws = d_workspace;
+    c->ws_bytes = bytes;
+    cudaGetDevice(&c->device);
+    plan(*cfg, true, &c->w, (char *)d_workspace);
+    c->w.n_scan = n_scan_for(cfg->batch, cfg->n_kv_heads, cfg->max_len);
+    if (cudaMemset(d_workspace, 0, plan(*cfg, true, nullptr, nullptr)) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        free(c);
+        return RETOPK_ERR_CUDA;
+    }
+    *out = c;
+    return RETOPK_OK;
+}
+
+int retopk_destroy(retopk_ctx *ctx)
+{
+    if (!ctx)
+        return RETOPK_ERR_INVALID;
+    free(ctx);
+    return RETOPK_OK;
+}
+
+int retopk_init_cache(retopk_ctx *ctx, const retopk_bf16 *q_last, const retopk_bf16 *k_cache,
+                      const int32_t *d_prompt_len, void *stream)
+{
+    if (!ctx || !q_last || !k_cache || !d_prompt_len)
+        return RETOPK_ERR_INVALID;
+    if (!aligned16(q_last) || !aligned16(k_cache))
+        return RETOPK_ERR_ALIGN;
+    cudaStream_t st = (cudaStream_t)stream;
+    const Work &w0 = ctx->w;
+    std::vector<int32_t> L0(w0.B);
+    if (cudaMemcpyAsync(L0.data(), d_prompt_len, sizeof(int32_t) * w0.B, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return RETOPK_ERR_CUDA;
+    for (int b = 0; b < w0.B; ++b)
+        if (L0[b] < w0.C || L0[b] > w0.max_len)
+            return RETOPK_ERR_INVALID;
+    // every head takes the exact path during initialisation
+    Work w = w0;
+    w.path = nullptr;
+    QSrc qs{q_last, (long long)w.Hq * w.C * kD, (long long)w.C * kD};
+    for (int c = 0; c < w.C; ++c) {
+        const int off = c + 1 - w.C;   // causal prefix 0..L0-C+c
+        QSrc qc{qs.q + (size_t)c * kD, qs.b_stride, qs.h_stride};
+        if (cudaMemsetAsync(w.hist, 0, (size_t)w.B * w.Hq * kHistBins * 4, st) != cudaSuccess)
+            return RETOPK_ERR_CUDA;
+        int e = run_scan(w, qc, k_cache, d_prompt_len, off, st);
+        if (e)
+            return e;
+        if (launch_filter(w, d_prompt_len, off, st) != cudaSuccess)
+            return RETOPK_ERR_CUDA;
+        if (launch_finalize(w, qc, k_cache, d_prompt_len, off, FIN_INIT, c, nullptr, nullptr, st) != cudaSuccess)
+            return RETOPK_ERR_CUDA;
+    }
+    return cuda_rc(launch_init_done(w0, st));
+}
+
+int retopk_append_kv(retopk_ctx *ctx, const retopk_bf16 *k_new, const retopk_bf16 *v_new,
+                     retopk_bf16 *k_cache, retopk_bf16 *v_cache, int32_t *d_seqlens, void *stream)
+{
+    if (!ctx || !k_new || !v_new || !k_cache || !v_cache || !d_seqlens)
+        return RETOPK_ERR_INVALID;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return RETOPK_ERR_ALIGN;
+    return cuda_rc(launch_append(ctx->w, k_new, v_new, k_cache, v_cache, d_seqlens, (cudaStream_t)stream));
+}
+
+int retopk_decode_step(retopk_ctx *ctx, const retopk_bf16 *q, const retopk_bf16 *k_cache,
+                       const retopk_bf16 *v_cache, const int32_t *d_seqlens, retopk_bf16 *out,
+                       void *stream)
+{
+    if (!ctx || !q || !k_cache || !v_cache || !d_seqlens || !out)
+        return RETOPK_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return RETOPK_ERR_ALIGN;
+    cudaStream_t st = (cudaStream_t)stream;
+    const Work &w = ctx->w;
+    QSrc qs{q, (long long)w.Hq * kD, kD};
+    if (launch_recall(w, q, d_seqlens, st) != cudaSuccess)
+        return RETOPK_ERR_CUDA;
+    if (launch_rerank(w, q, k_cache, d_seqlens, st) != cudaSuccess)
+        return RETOPK_ERR_CUDA;
+    int e = run_scan(w, qs, k_cache, d_seqlens, 0, st);
+    if (e)
+        return e;
+    if (launch_filter(w, d_seqlens, 0, st) != cudaSuccess)
+        return RETOPK_ERR_CUDA;
+    return cuda_rc(launch_finalize(w, qs, v_cache, d_seqlens, 0, FIN_DECODE, 0, out, nullptr, st));
+}
+
+int retopk_get_diagnostics(retopk_ctx *ctx, int32_t *path, float *rho_max, int32_t *topR, int32_t *M,
+                           int32_t *cand, int32_t *support, int32_t *sup_len, float *out_f32,
+                           void *stream)
+{
+    if (!ctx)
+        return RETOPK_ERR_INVALID;
+    cudaStream_t st = (cudaStream_t)stream;
+    const Work &w = ctx->w;
+    const size_t BH = (size_t)w.B * w.Hq;
+    cudaError_t e = cudaSuccess;
+    auto cp = [&](void *dst, const void *src, size_t n) {
+        if (dst && e == cudaSuccess)
+            e = cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToHost, st);
+    };
+    cp(path, w.path, BH * 4);
+    cp(rho_max, w.rho_max, BH * 4);
+    cp(topR, w.topR, BH * w.R * 4);
+    cp(M, w.M, BH * 4);
+    cp(support, w.support, BH * w.K * 4);
+    cp(sup_len, w.sup_len, BH * 4);
+    cp(out_f32, w.out_f32, BH * kD * 4);
+    if (cand && e == cudaSuccess) {
+        const size_t cap = (size_t)w.R * w.K + w.W;
+        e = cudaMemcpy2DAsync(cand, cap * 4, w.cand_idx, (size_t)w.cand_stride * 4, cap * 4, BH,
+                              cudaMemcpyDeviceToHost, st);
+    }
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess)
+        return RETOPK_ERR_CUDA;
+    if (cand) {
+        // entries past M_t (and every entry of exact heads) are not part of A_t
+        std::vector<int32_t> Mh(BH), ph(BH);
+        cudaMemcpy(Mh.data(), w.M, BH * 4, cudaMemcpyDeviceToHost);
+        cudaMemcpy(ph.data(), w.path, BH * 4, cudaMemcpyDeviceToHost);
+        const size_t cap = (size_t)w.R * w.K + w.W;
+        for (size_t i = 0; i < BH; ++i) {
+            const size_t m = ph[i] == RETOPK_PATH_REUSE ? std::min<size_t>(cap, (size_t)Mh[i]) : 0;
+            for (size_t j = m; j < cap; ++j)
+                cand[i * cap + j] = -1;
+        }
+    }
+    return RETOPK_OK;
+}
+
+int retopk_get_counters(retopk_ctx *ctx, int64_t counts[5], void *stream)
+{
+    if (!ctx || !counts)
+        return RETOPK_ERR_INVALID;
+    const Work &w = ctx->w;
+    std::vector<unsigned long long> h((size_t)w.B * CNT_WORDS);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(h.data(), w.counters, h.size() * 8, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return RETOPK_ERR_CUDA;
+    for (int i = 0; i < 5; ++i)
+        counts[i] = 0;
+    for (int b = 0; b < w.B; ++b) {
+        for (int i = 0; i < 4; ++i)
+            counts[i] += (int64_t)h[(size_t)b * CNT_WORDS + i];
+        counts[4] = std::max<int64_t>(counts[4], (int64_t)h[(size_t)b * CNT_WORDS + CNT_MAX_M]);
+    }
+    return RETOPK_OK;
+}
+
+size_t retopk_state_bytes(const retopk_ctx *ctx)
+{
+    if (!ctx)
+        return 0;
+    const Work &w = ctx->w;
+    const size_t BHC = (size_t)w.B * w.Hq * w.C;
+    return BHC * kD * 2 + BHC * w.K * 4 + BHC * 4 + (size_t)w.B * 3 * 4;
+}
+
+static int state_copy(retopk_ctx *ctx, void *host, size_t bytes, cudaStream_t st, bool to_host)
+{
+    const Work &w = ctx->w;
+    if (!host || bytes != retopk_state_bytes(ctx))
+        return RETOPK_ERR_STATE;
+    const size_t BHC = (size_t)w.B * w.Hq * w.C;
+    char *p = (char *)host;
+    const cudaMemcpyKind kd = to_host ? cudaMemcpyDeviceToHost : cudaMemcpyHostToDevice;
+    cudaError_t e = cudaSuccess;
+    auto cp = [&](void *dev, size_t n) {
+        if (e == cudaSuccess)
+            e = to_host ? cudaMemcpyAsync(p, dev, n, kd, st) : cudaMemcpyAsync(dev, p, n, kd, st);
+        p += n;
+    };
+    cp(w.fifo_q, BHC * kD * 2);
+    cp(w.fifo_sup, BHC * w.K * 4);
+    cp(w.fifo_len, BHC * 4);
+    // seq words: the device keeps 4 per sequence, the buffer 3
+    std::vector<int32_t> seq((size_t)w.B * SEQ_WORDS);
+    if (e == cudaSuccess && to_host) {
+        e = cudaMemcpyAsync(seq.data(), w.seq, seq.size() * 4, cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess)
+            e = cudaStreamSynchronize(st);
+        for (int b = 0; b < w.B; ++b)
+            memcpy(p + b * 12, &seq[(size_t)b * SEQ_WORDS], 12);
+    } else if (e == cudaSuccess) {
+        for (int b = 0; b < w.B; ++b) {
+            memcpy(&seq[(size_t)b * SEQ_WORDS], p + b * 12, 12);
+            seq[(size_t)b * SEQ_WORDS + SEQ_DONE] = 0;
+        }
+        e = cudaMemcpyAsync(w.seq, seq.data(), seq.size() * 4, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess)
+            e = cudaStreamSynchronize(st);
+    }
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(st);
+    return cuda_rc(e);
+}
+
+int retopk_export_state(retopk_ctx *ctx, void *host_buf, size_t bytes, void *stream)
+{
+    if (!ctx)
+        return RETOPK_ERR_INVALID;
+    return state_copy(ctx, host_buf, bytes, (cudaStream_t)stream, true);
+}
+
+int retopk_import_state(retopk_ctx *ctx, const void *host_buf, size_t bytes, void *stream)
+{
+    if (!ctx)
+        return RETOPK_ERR_INVALID;
+    const Work &w = ctx->w;
+    // validate before touching the device: slots, counts and support indices
+    const size_t BHC = (size_t)w.B * w.Hq * w.C;
+    if (!host_buf || bytes != retopk_state_bytes(ctx))
+        return RETOPK_ERR_STATE;
+    const char *p = (const char *)host_buf;
+    const int32_t *len = (const int32_t *)(p + BHC * kD * 2 + BHC * w.K * 4);
+    const int32_t *seq = len + BHC;
+    for (size_t i = 0; i < BHC; ++i)
+        if (len[i] < 0 || len[i] > w.K)
+            return RETOPK_ERR_STATE;
+    for (int b = 0; b < w.B; ++b)
+        if (seq[b * 3] < 0 || seq[b * 3] >= w.C || seq[b * 3 + 1] < 0 || seq[b * 3 + 1] > w.C ||
+            seq[b * 3 + 2] < 0)
+            return RETOPK_ERR_STATE;
+    return state_copy(ctx, const_cast<void *>(host_buf), bytes, (cudaStream_t)stream, false);
+}
+
+int retopk_get_status(retopk_ctx *ctx, uint32_t *bits, int clear, void *stream)
+{
+    if (!ctx || !bits)
+        return RETOPK_ERR_INVALID;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(bits, ctx->w.status, 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && clear)
+        e = cudaMemsetAsync(ctx->w.status, 0, 4, st);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(st);
+    return cuda_rc(e);
+}
+
+const char *retopk_strerror(int code)
+{
+    switch (code) {
+    case RETOPK_OK: return "ok";
+    case RETOPK_ERR_INVALID: return "invalid argument";
+    case RETOPK_ERR_UNSUPPORTED: return "unsupported size (head_dim must be 128; group, K, C or max_len too large)";
+    case RETOPK_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
+    case RETOPK_ERR_CUDA: return "CUDA runtime error";
+    case RETOPK_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
+    case RETOPK_ERR_STATE: return "state buffer of the wrong size or with invalid contents";
+    default: return "unknown error";
+    }
+}
+
+size_t exact_topk_workspace_bytes(int B, int Hq, int Hkv, int d, int max_len, int K)
+{
+    if (check_dims(B, Hq, Hkv, d, max_len, K))
+        return 0;
+    retopk_config c{B, Hq, Hkv, d, max_len, K, 1, 0, 1, 0, 0.f};
+    return plan(c, false, nullptr, nullptr);
+}
+
+int exact_topk_attention_step(const retopk_bf16 *q, const retopk_bf16 *k_cache, const retopk_bf16 *v_cache,
+                              const int32_t *d_seqlens, int B, int Hq, int Hkv, int d, int max_len, int K,
+                              retopk_bf16 *out, int32_t *idx_out, void *d_workspace, size_t bytes,
+                              void *stream)
+{
+    int e = check_dims(B, Hq, Hkv, d, max_len, K);
+    if (e)
+        return e;
+    if (!q || !k_cache || !v_cache || !d_seqlens || !out || !d_workspace)
+        return RETOPK_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return RETOPK_ERR_ALIGN;
+    retopk_config c{B, Hq, Hkv, d, max_len, K, 1, 0, 1, 0, 0.f};
+    const size_t need = plan(c, false, nullptr, nullptr);
+    if (((uintptr_t)d_workspace & (kAlign - 1)) != 0 || bytes < need)
+        return RETOPK_ERR_WORKSPACE;
+    if ((e = ensure_configured()))
+        return e;
+    Work w;
+    plan(c, false, &w, (char *)d_workspace);
+    w.n_scan = n_scan_for(B, Hkv, max_len);
+    w.out_f32 = nullptr;
+    w.support = nullptr;
+    cudaStream_t st = (cudaStream_t)stream;
+    QSrc qs{q, (long long)Hq * kD, kD};
+    if (cudaMemsetAsync(w.hist, 0, (size_t)B * Hq * kHistBins * 4, st) != cudaSuccess)
+        return RETOPK_ERR_CUDA;
+    if ((e = run_scan(w, qs, k_cache, d_seqlens, 0, st)))
+        return e;
+    if (launch_filter(w, d_seqlens, 0, st) != cudaSuccess)
+        return RETOPK_ERR_CUDA;
+    return cuda_rc(launch_finalize(w, qs, v_cache, d_seqlens, 0, FIN_EXACT, 0, out, idx_out, st));
+}
+
+int retopk_profile_enable(int on)
+{
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    g_prof.on = on != 0;
+    return RETOPK_OK;
+}
+
+int retopk_profile_read(int64_t *scan_launches, double *scan_ms)
+{
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev;
+    {
+        std::lock_guard<std::mutex> lk(g_prof.mu);
+        ev.swap(g_prof.ev);
+    }
+    double ms = 0.0;
+    int rc = RETOPK_OK;
+    for (auto &p : ev) {
+        float t = 0.f;
+        if (cudaEventSynchronize(p.second) != cudaSuccess || cudaEventElapsedTime(&t, p.first, p.second) != cudaSuccess)
+            rc = RETOPK_ERR_CUDA;
+        ms += t;
+        cudaEventDestroy(p.first);
+        cudaEventDestroy(p.second);
+    }
+    if (scan_launches)
+        *scan_launches = (int64_t)ev.size();
+    if (scan_ms)
+        *scan_ms = ms;
+    return rc;
+}
+
+}  // extern "C"
