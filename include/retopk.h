@@ -57,6 +57,8 @@ enum {
 #define RETOPK_STATUS_BAD_INDEX   0x1u  /* cached support index outside [0, L)      */
 #define RETOPK_STATUS_KV_FULL     0x2u  /* append with seqlens[b] == max_len        */
 #define RETOPK_STATUS_NONFINITE   0x4u  /* a non-finite score was produced          */
+#define RETOPK_STATUS_TIMEOUT     0x8u  /* a bounded pipeline wait expired (the step's
+                                           results are not valid)                  */
 
 /* Path codes reported per (sequence, query head), Eq. (13). */
 #define RETOPK_PATH_REUSE    0
@@ -66,8 +68,9 @@ enum {
 /* ReTopK hyper-parameters (§Reliable Reuse, §Implementation settings):
  * K support size, C cache capacity, W recent window, R retrieved entries,
  * T_r refresh period (0 disables refresh), tau similarity threshold.
- * Limits: d = 128; 1 <= Hq/Hkv <= 32; 1 <= K <= 4096; 1 <= R <= C <= 256;
- * 0 <= W; max_len <= 2^20 (the candidate bitmap lives in shared memory). */
+ * Limits: d = 128; 1 <= Hq/Hkv <= 16; B * Hkv <= 512; 1 <= K <= 4096;
+ * 1 <= R <= C <= 256; 0 <= W; R*K + W <= 20480; max_len <= 2^20 (the
+ * candidate bitmap and list live in shared memory). */
 typedef struct retopk_config {
     int32_t batch;        /* B                                                  */
     int32_t n_q_heads;    /* Hq                                                 */
@@ -165,6 +168,10 @@ int retopk_import_state(retopk_ctx *ctx, const void *host_buf, size_t bytes, voi
 int retopk_get_status(retopk_ctx *ctx, uint32_t *bits, int clear, void *stream);
 
 const char *retopk_strerror(int code);
+
+/* The CUDA runtime's message for the last CUDA error that made a call of this
+ * thread return RETOPK_ERR_CUDA (a static string; never NULL). */
+const char *retopk_cuda_error_string(void);
 
 /* ---- Exact Top-K (stateless) -------------------------------------------- */
 

@@ -13,7 +13,7 @@
 namespace retopk {
 cudaError_t configure_scan();
 cudaError_t configure_select();
-cudaError_t configure_recall(int bytes);
+cudaError_t configure_recall();
 }  // namespace retopk
 
 using namespace retopk;
@@ -44,6 +44,16 @@ struct Layout {
     }
 };
 
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+int cuda_rc(cudaError_t e)
+{
+    if (e == cudaSuccess)
+        return RETOPK_OK;
+    g_last_cuda_error = e;
+    return RETOPK_ERR_CUDA;
+}
+
 int sm_count()
 {
     static int n = 0;
@@ -65,9 +75,9 @@ int ensure_configured()
         if (err == cudaSuccess)
             err = configure_select();
         if (err == cudaSuccess)
-            err = configure_recall(kMaxLen / 8);
+            err = configure_recall();
     });
-    return err == cudaSuccess ? RETOPK_OK : RETOPK_ERR_CUDA;
+    return cuda_rc(err);
 }
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
@@ -76,7 +86,7 @@ int n_filter_for(int max_len) { return std::min(kMaxSeg, std::max(1, (max_len + 
 
 int cand_stride_for(int max_len, int n_filter, int RKW)
 {
-    const int seg = (((max_len + n_filter - 1) / n_filter) + 255) & ~255;
+    const int seg = (((max_len + n_filter - 1) / n_filter) + 15) & ~15;
     const int s = std::max(seg * n_filter, RKW);
     return (s + 63) & ~63;
 }
@@ -101,6 +111,7 @@ size_t plan(const retopk_config &c, bool stateful, Work *w, char *base)
     const int RKW = stateful ? c.R * c.K + c.W : 0;
     x.cand_stride = cand_stride_for(c.max_len, x.n_filter, RKW);
     x.n_rerank = stateful ? std::min(32, std::max(1, (RKW + 255) / 256)) : 1;
+    x.sc_stride = (c.max_len + 15) & ~15;
     const size_t BH = (size_t)c.batch * c.n_q_heads;
     Layout L;
     size_t o_fq = 0, o_fs = 0, o_fl = 0, o_seq = 0, o_cnt = 0, o_path = 0, o_rho = 0, o_topr = 0;
@@ -118,7 +129,7 @@ size_t plan(const retopk_config &c, bool stateful, Work *w, char *base)
     const size_t o_ci = L.add(BH * x.cand_stride * 4);
     const size_t o_ck = L.add(BH * x.cand_stride * 4);
     const size_t o_sg = L.add(BH * x.n_filter * 4);
-    const size_t o_sc = L.add(BH * (size_t)c.max_len * 4);
+    const size_t o_sc = L.add(BH * (size_t)x.sc_stride * 4);
     const size_t o_h = L.add(BH * kHistBins * 4);
     const size_t o_sup = L.add(BH * c.K * 4);
     const size_t o_sl = L.add(BH * 4);
@@ -157,7 +168,7 @@ int check_dims(int B, int Hq, int Hkv, int d, int max_len, int K)
         return RETOPK_ERR_INVALID;
     if (Hq % Hkv != 0)
         return RETOPK_ERR_INVALID;
-    if (d != kD || Hq / Hkv > kMaxGroup || max_len > kMaxLen || K > kMaxK)
+    if (d != kD || Hq / Hkv > kMaxGroup || max_len > kMaxLen || K > kMaxK || (long long)B * Hkv > kMaxSeqGroups)
         return RETOPK_ERR_UNSUPPORTED;
     return RETOPK_OK;
 }
@@ -171,12 +182,13 @@ int check_cfg(const retopk_config *c)
         return e;
     if (c->C < 1 || c->C > kMaxC || c->R < 1 || c->R > c->C || c->W < 0 || c->T_r < 0)
         return RETOPK_ERR_INVALID;
+    if ((long long)c->R * c->K + c->W > kMaxCand)
+        return RETOPK_ERR_UNSUPPORTED;
     if (isnan(c->tau))
         return RETOPK_ERR_INVALID;
     return RETOPK_OK;
 }
 
-int cuda_rc(cudaError_t e) { return e == cudaSuccess ? RETOPK_OK : RETOPK_ERR_CUDA; }
 
 // ---- optional scan timing -------------------------------------------------
 struct Prof {
@@ -187,46 +199,29 @@ struct Prof {
     double done_ms = 0.0;
 } g_prof;
 
-void prof_begin(cudaStream_t st, cudaEvent_t *a)
-{
-    *a = nullptr;
-    if (!g_prof.on)
-        return;
-    if (cudaEventCreate(a) == cudaSuccess)
-        cudaEventRecord(*a, st);
-    else
-        *a = nullptr;
-}
-
-void prof_end(cudaStream_t st, cudaEvent_t a)
-{
-    if (!a)
-        return;
-    cudaEvent_t b;
-    if (cudaEventCreate(&b) != cudaSuccess) {
-        cudaEventDestroy(a);
-        return;
-    }
-    cudaEventRecord(b, st);
-    std::lock_guard<std::mutex> lk(g_prof.mu);
-    g_prof.ev.emplace_back(a, b);
-}
-
 int run_scan(const Work &w, QSrc q, const uint16_t *k, const int32_t *sl, int off, cudaStream_t st)
 {
-    cudaEvent_t ev;
-    prof_begin(st, &ev);
-    const cudaError_t e = launch_scan(w, q, k, sl, off, st);
-    prof_end(st, ev);
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (g_prof.on) {
+        if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+            if (e0)
+                cudaEventDestroy(e0);
+            e0 = e1 = nullptr;
+        }
+    }
+    const cudaError_t e = launch_scan(w, q, k, sl, off, st, e0, e1);
+    if (e0) {
+        std::lock_guard<std::mutex> lk(g_prof.mu);
+        g_prof.ev.emplace_back(e0, e1);
+    }
     return cuda_rc(e);
 }
 
+// The scan is persistent: one CTA per SM shares the tiles of every active group.
 int n_scan_for(int B, int Hkv, int max_len)
 {
-    const int target = sm_count() * scan_ctas_per_sm();
-    int n = (target + B * Hkv - 1) / (B * Hkv);
-    const int by_len = (max_len + 255) / 256;
-    return std::max(1, std::min(n, by_len));
+    const long long tiles = (long long)B * Hkv * ((max_len + 127) / 128);
+    return (int)std::max(1LL, std::min<long long>(sm_count() * scan_ctas_per_sm(), tiles));
 }
 
 }  // namespace
@@ -260,10 +255,12 @@ int retopk_create(const retopk_config *cfg, void *d_workspace, size_t bytes, ret
     cudaGetDevice(&c->device);
     plan(*cfg, true, &c->w, (char *)d_workspace);
     c->w.n_scan = n_scan_for(cfg->batch, cfg->n_kv_heads, cfg->max_len);
-    if (cudaMemset(d_workspace, 0, plan(*cfg, true, nullptr, nullptr)) != cudaSuccess ||
-        cudaDeviceSynchronize() != cudaSuccess) {
+    cudaError_t ce = cudaMemset(d_workspace, 0, plan(*cfg, true, nullptr, nullptr));
+    if (ce == cudaSuccess)
+        ce = cudaDeviceSynchronize();
+    if (ce != cudaSuccess) {
         free(c);
-        return RETOPK_ERR_CUDA;
+        return cuda_rc(ce);
     }
     *out = c;
     return RETOPK_OK;
@@ -287,9 +284,11 @@ int retopk_init_cache(retopk_ctx *ctx, const retopk_bf16 *q_last, const retopk_b
     cudaStream_t st = (cudaStream_t)stream;
     const Work &w0 = ctx->w;
     std::vector<int32_t> L0(w0.B);
-    if (cudaMemcpyAsync(L0.data(), d_prompt_len, sizeof(int32_t) * w0.B, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        cudaStreamSynchronize(st) != cudaSuccess)
-        return RETOPK_ERR_CUDA;
+    cudaError_t ce = cudaMemcpyAsync(L0.data(), d_prompt_len, sizeof(int32_t) * w0.B, cudaMemcpyDeviceToHost, st);
+    if (ce == cudaSuccess)
+        ce = cudaStreamSynchronize(st);
+    if (ce != cudaSuccess)
+        return cuda_rc(ce);
     for (int b = 0; b < w0.B; ++b)
         if (L0[b] < w0.C || L0[b] > w0.max_len)
             return RETOPK_ERR_INVALID;
@@ -300,15 +299,15 @@ int retopk_init_cache(retopk_ctx *ctx, const retopk_bf16 *q_last, const retopk_b
     for (int c = 0; c < w.C; ++c) {
         const int off = c + 1 - w.C;   // causal prefix 0..L0-C+c
         QSrc qc{qs.q + (size_t)c * kD, qs.b_stride, qs.h_stride};
-        if (cudaMemsetAsync(w.hist, 0, (size_t)w.B * w.Hq * kHistBins * 4, st) != cudaSuccess)
-            return RETOPK_ERR_CUDA;
-        int e = run_scan(w, qc, k_cache, d_prompt_len, off, st);
-        if (e)
+        int e;
+        if ((e = cuda_rc(cudaMemsetAsync(w.hist, 0, (size_t)w.B * w.Hq * kHistBins * 4, st))))
             return e;
-        if (launch_filter(w, d_prompt_len, off, st) != cudaSuccess)
-            return RETOPK_ERR_CUDA;
-        if (launch_finalize(w, qc, k_cache, d_prompt_len, off, FIN_INIT, c, nullptr, nullptr, st) != cudaSuccess)
-            return RETOPK_ERR_CUDA;
+        if ((e = run_scan(w, qc, k_cache, d_prompt_len, off, st)))
+            return e;
+        if ((e = cuda_rc(launch_filter(w, d_prompt_len, off, st))))
+            return e;
+        if ((e = cuda_rc(launch_finalize(w, qc, k_cache, d_prompt_len, off, FIN_INIT, c, nullptr, nullptr, st))))
+            return e;
     }
     return cuda_rc(launch_init_done(w0, st));
 }
@@ -334,15 +333,13 @@ int retopk_decode_step(retopk_ctx *ctx, const retopk_bf16 *q, const retopk_bf16 
     cudaStream_t st = (cudaStream_t)stream;
     const Work &w = ctx->w;
     QSrc qs{q, (long long)w.Hq * kD, kD};
-    if (launch_recall(w, q, d_seqlens, st) != cudaSuccess)
-        return RETOPK_ERR_CUDA;
-    if (launch_rerank(w, q, k_cache, d_seqlens, st) != cudaSuccess)
-        return RETOPK_ERR_CUDA;
-    int e = run_scan(w, qs, k_cache, d_seqlens, 0, st);
-    if (e)
+    int e;
+    if ((e = cuda_rc(launch_recall(w, q, k_cache, d_seqlens, st))))
         return e;
-    if (launch_filter(w, d_seqlens, 0, st) != cudaSuccess)
-        return RETOPK_ERR_CUDA;
+    if ((e = run_scan(w, qs, k_cache, d_seqlens, 0, st)))
+        return e;
+    if ((e = cuda_rc(launch_filter(w, d_seqlens, 0, st))))
+        return e;
     return cuda_rc(launch_finalize(w, qs, v_cache, d_seqlens, 0, FIN_DECODE, 0, out, nullptr, st));
 }
 
@@ -375,7 +372,7 @@ int retopk_get_diagnostics(retopk_ctx *ctx, int32_t *path, float *rho_max, int32
     if (e == cudaSuccess)
         e = cudaStreamSynchronize(st);
     if (e != cudaSuccess)
-        return RETOPK_ERR_CUDA;
+        return cuda_rc(e);
     if (cand) {
         // entries past M_t (and every entry of exact heads) are not part of A_t
         std::vector<int32_t> Mh(BH), ph(BH);
@@ -398,9 +395,11 @@ int retopk_get_counters(retopk_ctx *ctx, int64_t counts[5], void *stream)
     const Work &w = ctx->w;
     std::vector<unsigned long long> h((size_t)w.B * CNT_WORDS);
     cudaStream_t st = (cudaStream_t)stream;
-    if (cudaMemcpyAsync(h.data(), w.counters, h.size() * 8, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        cudaStreamSynchronize(st) != cudaSuccess)
-        return RETOPK_ERR_CUDA;
+    cudaError_t ce = cudaMemcpyAsync(h.data(), w.counters, h.size() * 8, cudaMemcpyDeviceToHost, st);
+    if (ce == cudaSuccess)
+        ce = cudaStreamSynchronize(st);
+    if (ce != cudaSuccess)
+        return cuda_rc(ce);
     for (int i = 0; i < 5; ++i)
         counts[i] = 0;
     for (int b = 0; b < w.B; ++b) {
@@ -501,6 +500,11 @@ int retopk_get_status(retopk_ctx *ctx, uint32_t *bits, int clear, void *stream)
     return cuda_rc(e);
 }
 
+const char *retopk_cuda_error_string(void)
+{
+    return g_last_cuda_error == cudaSuccess ? "no CUDA error recorded" : cudaGetErrorString(g_last_cuda_error);
+}
+
 const char *retopk_strerror(int code)
 {
     switch (code) {
@@ -548,12 +552,12 @@ int exact_topk_attention_step(const retopk_bf16 *q, const retopk_bf16 *k_cache, 
     w.support = nullptr;
     cudaStream_t st = (cudaStream_t)stream;
     QSrc qs{q, (long long)Hq * kD, kD};
-    if (cudaMemsetAsync(w.hist, 0, (size_t)B * Hq * kHistBins * 4, st) != cudaSuccess)
-        return RETOPK_ERR_CUDA;
+    if ((e = cuda_rc(cudaMemsetAsync(w.hist, 0, (size_t)B * Hq * kHistBins * 4, st))))
+        return e;
     if ((e = run_scan(w, qs, k_cache, d_seqlens, 0, st)))
         return e;
-    if (launch_filter(w, d_seqlens, 0, st) != cudaSuccess)
-        return RETOPK_ERR_CUDA;
+    if ((e = cuda_rc(launch_filter(w, d_seqlens, 0, st))))
+        return e;
     return cuda_rc(launch_finalize(w, qs, v_cache, d_seqlens, 0, FIN_EXACT, 0, out, idx_out, st));
 }
 

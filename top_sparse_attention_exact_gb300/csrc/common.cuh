@@ -19,6 +19,8 @@ constexpr int kMaxK = 4096;
 constexpr int kMaxC = 256;
 constexpr int kStageCap = 12288;    // candidates staged in shared memory by finalize
 constexpr int kMaxSeg = 64;         // filter CTAs (segments) per head
+constexpr int kMaxSeqGroups = 512;  // B * Hkv handled by one scan launch
+constexpr int kMaxCand = 20480;     // R*K + W (the candidate list lives in smem)
 
 // Per-sequence control words.
 enum { SEQ_HEAD = 0, SEQ_COUNT = 1, SEQ_TDEC = 2, SEQ_DONE = 3, SEQ_WORDS = 4 };
@@ -32,7 +34,8 @@ struct Work {
     int cand_stride;   // per-head capacity of cand_idx / cand_key
     int n_filter;      // filter CTAs (segments) per head
     int n_scan;        // scan CTAs per (b, h_kv)
-    int n_rerank;      // rerank CTAs per head
+    int n_rerank;      // recall/rerank CTAs per head
+    int sc_stride;     // row stride of `scores` (max_len rounded up to 16)
     // query-support cache (decode contexts only)
     uint16_t *fifo_q;
     int32_t *fifo_sup;
@@ -47,7 +50,7 @@ struct Work {
     int32_t *cand_idx;   // [B*Hq*cand_stride]
     uint32_t *cand_key;  // [B*Hq*cand_stride]
     int32_t *seg_count;  // [B*Hq*n_filter]
-    float *scores;       // [B*Hq*max_len]
+    float *scores;       // [B*Hq*sc_stride]
     uint32_t *hist;      // [B*Hq*kHistBins]
     int32_t *support;    // [B*Hq*K]
     int32_t *sup_len;    // [B*Hq]
@@ -105,15 +108,15 @@ struct QSrc {              // where the query of (b, h) lives
     long long b_stride, h_stride;   // in elements
 };
 
+// ev0 / ev1 (optional) are recorded immediately around the kernel launch.
 cudaError_t launch_scan(const Work &w, QSrc q, const uint16_t *k_cache, const int32_t *seqlens,
-                        int len_off, cudaStream_t st);
+                        int len_off, cudaStream_t st, cudaEvent_t ev0 = nullptr, cudaEvent_t ev1 = nullptr);
 cudaError_t launch_filter(const Work &w, const int32_t *seqlens, int len_off, cudaStream_t st);
 cudaError_t launch_finalize(const Work &w, QSrc q, const uint16_t *v_cache, const int32_t *seqlens,
                             int len_off, int mode, int init_slot, uint16_t *out, int32_t *idx_out,
                             cudaStream_t st);
-cudaError_t launch_recall(const Work &w, const uint16_t *q, const int32_t *seqlens, cudaStream_t st);
-cudaError_t launch_rerank(const Work &w, const uint16_t *q, const uint16_t *k_cache,
-                          const int32_t *seqlens, cudaStream_t st);
+cudaError_t launch_recall(const Work &w, const uint16_t *q, const uint16_t *k_cache, const int32_t *seqlens,
+                          cudaStream_t st);
 cudaError_t launch_append(const Work &w, const uint16_t *k_new, const uint16_t *v_new,
                           uint16_t *k_cache, uint16_t *v_cache, int32_t *seqlens, cudaStream_t st);
 cudaError_t launch_init_done(const Work &w, cudaStream_t st);

@@ -8,9 +8,11 @@
 //                  window) (Eqs. (8)-(9)) built in a shared-memory bitmap of
 //                  L bits and emitted in ascending order.  Exact heads get
 //                  their score histogram cleared for the scan.
-//   rerank_kernel  exact scores q_t . k_i / sqrt(d) of the candidate keys only
-//                  (Eq. (10)), gathered straight from the K cache with
-//                  16-byte loads (half a warp per key row).
+//                  The same kernel then computes the exact scores
+//                  q_t . k_i / sqrt(d) of the candidate keys only (Eq. (10)),
+//                  gathered straight from the K cache with 16-byte loads (half
+//                  a warp per key row); several CTAs share one head's
+//                  candidates.
 //   append_kernel  writes the new token's key and value rows and advances L.
 #include "common.cuh"
 
@@ -19,28 +21,46 @@ namespace retopk {
 struct RecallArgs {
     Work w;
     const uint16_t *q;
+    const uint16_t *k;
     const int32_t *seqlens;
+    float scale;
 };
 
-__global__ void __launch_bounds__(256) recall_kernel(RecallArgs a)
+constexpr int kRecallThreads = 256;
+constexpr int kRerankRows = 8;       // key rows per half-warp per round
+
+// grid (n_rerank, B*Hq).  Every CTA of a head recomputes the (cheap, exactly
+// reproducible) recall and candidate set; CTA x then scores candidates
+// [x*per, (x+1)*per).  CTA 0 publishes path, rho_max, R_t, M_t and A_t.
+__global__ void __launch_bounds__(kRecallThreads) recall_kernel(RecallArgs a)
 {
-    extern __shared__ uint32_t bitmap[];
+    extern __shared__ uint32_t rsm[];   // bitmap [ceil(L/32)] then A_t [R*K+W]
     __shared__ float qf[kD];
     __shared__ float rho[kMaxC];
     __shared__ int topr[kMaxC];
+    __shared__ int flen[kMaxC];
+    __shared__ float dot_s[kMaxC];
+    __shared__ float nrm_s[kMaxC];
     __shared__ int warp_tot[9];
     __shared__ float nq_s;
     __shared__ int path_s;
     const Work &w = a.w;
-    const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int b = bh / w.Hq;
+    const int bh = blockIdx.y, split = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = bh / w.Hq, hk = (bh % w.Hq) / w.G;
     const int L = seq_len(a.seqlens, b, 0, w.max_len);
     const int *sq = w.seq + b * SEQ_WORDS;
     const int head = sq[SEQ_HEAD], count = sq[SEQ_COUNT];
     const int t_dec = sq[SEQ_TDEC] + 1;
+    uint32_t *bitmap = rsm;
+    const int nwords = (L + 31) >> 5;
+    int32_t *cand_s = reinterpret_cast<int32_t *>(rsm + ((w.max_len + 31) >> 5));
 
     if (tid < kD)
         qf[tid] = __uint_as_float(((uint32_t)a.q[(size_t)bh * kD + tid]) << 16);
+    for (int c = tid; c < count; c += kRecallThreads) {
+        const int slot = ((head - count + c) % w.C + w.C) % w.C;
+        flen[c] = w.fifo_len[(size_t)bh * w.C + slot];
+    }
     __syncthreads();
     if (warp == 0) {
         float s = 0.f;
@@ -51,24 +71,39 @@ __global__ void __launch_bounds__(256) recall_kernel(RecallArgs a)
         if (lane == 0)
             nq_s = s;
     }
+    // Eq. (6): rho_c = D(q, q_c) / sqrt(D(q,q) D(q_c,q_c)), live entry c oldest
+    // first; each warp loads up to 4 cached queries at once
+    for (int c0 = warp * 4; c0 < count; c0 += 8 * 4) {
+        uint2 raw[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u;
+            const int slot = ((head - count + c) % w.C + w.C) % w.C;
+            raw[u] = (c < count) ? *reinterpret_cast<const uint2 *>(w.fifo_q + ((size_t)bh * w.C + slot) * kD + lane * 4)
+                                 : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float x0 = bf16lo(raw[u].x), x1 = bf16hi(raw[u].x), x2 = bf16lo(raw[u].y), x3 = bf16hi(raw[u].y);
+            float dqc = qf[lane * 4] * x0 + qf[lane * 4 + 1] * x1 + qf[lane * 4 + 2] * x2 + qf[lane * 4 + 3] * x3;
+            float ncc = x0 * x0 + x1 * x1 + x2 * x2 + x3 * x3;
+            dqc = warp_sum(dqc);
+            ncc = warp_sum(ncc);
+            if (lane == 0 && c0 + u < count) {
+                dot_s[c0 + u] = dqc;
+                nrm_s[c0 + u] = ncc;
+            }
+        }
+    }
     __syncthreads();
     const float nq = nq_s;
-    // Eq. (6): rho_c = D(q, q_c) / sqrt(D(q,q) D(q_c,q_c)), live entry c oldest first
-    for (int c = warp; c < count; c += 8) {
-        const int slot = ((head - count + c) % w.C + w.C) % w.C;
-        const uint2 raw = *reinterpret_cast<const uint2 *>(w.fifo_q + ((size_t)bh * w.C + slot) * kD + lane * 4);
-        const float x0 = bf16lo(raw.x), x1 = bf16hi(raw.x), x2 = bf16lo(raw.y), x3 = bf16hi(raw.y);
-        float dqc = qf[lane * 4] * x0 + qf[lane * 4 + 1] * x1 + qf[lane * 4 + 2] * x2 + qf[lane * 4 + 3] * x3;
-        float ncc = x0 * x0 + x1 * x1 + x2 * x2 + x3 * x3;
-        dqc = warp_sum(dqc);
-        ncc = warp_sum(ncc);
-        if (lane == 0)
-            rho[c] = (nq > 0.f && ncc > 0.f) ? (float)((double)dqc / sqrt((double)nq * (double)ncc))
-                                              : -INFINITY;
+    for (int c = tid; c < count; c += kRecallThreads) {
+        const float ncc = nrm_s[c], dqc = dot_s[c];
+        rho[c] = (nq > 0.f && ncc > 0.f) ? (float)((double)dqc / sqrt((double)nq * (double)ncc)) : -INFINITY;
     }
     __syncthreads();
     // Eq. (7): Top-R by (rho desc, older first); rank by counting
-    for (int c = tid; c < count; c += blockDim.x) {
+    for (int c = tid; c < count; c += kRecallThreads) {
         const float r = rho[c];
         int rank = 0;
         for (int c2 = 0; c2 < count; ++c2) {
@@ -84,50 +119,64 @@ __global__ void __launch_bounds__(256) recall_kernel(RecallArgs a)
         const bool refresh = (w.T_r > 0) && (t_dec % w.T_r == 0);
         const int p = refresh ? RETOPK_PATH_REFRESH : (!(rmax >= w.tau) ? RETOPK_PATH_FALLBACK : RETOPK_PATH_REUSE);
         path_s = p;
-        w.path[bh] = p;
-        w.rho_max[bh] = rmax;
+        if (split == 0) {
+            w.path[bh] = p;
+            w.rho_max[bh] = rmax;
+        }
     }
-    for (int r = tid; r < w.R; r += blockDim.x)
-        w.topR[(size_t)bh * w.R + r] = r < count ? topr[r] : -1;
-    __syncthreads();
-    if (path_s != RETOPK_PATH_REUSE) {
-        uint32_t *hg = w.hist + (size_t)bh * kHistBins;
-        for (int i = tid; i < kHistBins; i += blockDim.x)
-            hg[i] = 0u;
-        if (tid == 0)
-            w.M[bh] = L;
-        return;
-    }
+    if (split == 0)
+        for (int r = tid; r < w.R; r += kRecallThreads)
+            w.topR[(size_t)bh * w.R + r] = r < count ? topr[r] : -1;
     // Eqs. (8)-(9): bitmap union of the window and the retrieved supports
-    const int nwords = (L + 31) >> 5;
-    for (int i = tid; i < nwords; i += blockDim.x)
+    for (int i = tid; i < nwords; i += kRecallThreads)
         bitmap[i] = 0u;
     __syncthreads();
+    if (path_s != RETOPK_PATH_REUSE) {
+        if (split == 0) {
+            uint32_t *hg = w.hist + (size_t)bh * kHistBins;
+            for (int i = tid; i < kHistBins; i += kRecallThreads)
+                hg[i] = 0u;
+            if (tid == 0)
+                w.M[bh] = L;
+        }
+        return;
+    }
     const int lo = max(0, L - w.W);
-    for (int i = lo + tid; i < L; i += blockDim.x)
+    for (int i = lo + tid; i < L; i += kRecallThreads)
         atomicOr(&bitmap[i >> 5], 1u << (i & 31));
     const int nr = min(w.R, count);
     for (int r = 0; r < nr; ++r) {
-        const int slot = ((head - count + topr[r]) % w.C + w.C) % w.C;
-        const size_t e = (size_t)bh * w.C + slot;
-        const int len = w.fifo_len[e];
-        const int32_t *sp = w.fifo_sup + e * w.K;
-        for (int j = tid; j < len; j += blockDim.x) {
-            const int i = sp[j];
-            if (i >= 0 && i < L)
-                atomicOr(&bitmap[i >> 5], 1u << (i & 31));
-            else
-                atomicOr(w.status, RETOPK_STATUS_BAD_INDEX);
+        const int c = topr[r];
+        const int slot = ((head - count + c) % w.C + w.C) % w.C;
+        const int len = flen[c];
+        const int32_t *sp = w.fifo_sup + ((size_t)bh * w.C + slot) * w.K;
+        for (int j0 = tid; j0 < len; j0 += kRecallThreads * 4) {
+            int id[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u * kRecallThreads;
+                id[u] = j < len ? sp[j] : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u * kRecallThreads;
+                if (j < len) {
+                    const int i = id[u];
+                    if (i >= 0 && i < L)
+                        atomicOr(&bitmap[i >> 5], 1u << (i & 31));
+                    else if (split == 0)
+                        atomicOr(w.status, RETOPK_STATUS_BAD_INDEX);
+                }
+            }
         }
     }
     __syncthreads();
-    // ascending emission: each thread owns a contiguous run of words
-    const int wpt = (nwords + blockDim.x - 1) / blockDim.x;
+    // ascending emission into shared memory: each thread owns a run of words
+    const int wpt = (nwords + kRecallThreads - 1) / kRecallThreads;
     const int w0 = min(nwords, tid * wpt), w1 = min(nwords, w0 + wpt);
     int mine = 0;
     for (int i = w0; i < w1; ++i)
         mine += __popc(bitmap[i]);
-    // block exclusive scan of `mine` (8 warps)
     int x = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -140,7 +189,7 @@ __global__ void __launch_bounds__(256) recall_kernel(RecallArgs a)
     __syncthreads();
     if (tid == 0) {
         int acc = 0;
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < kRecallThreads / 32; ++i) {
             const int v = warp_tot[i];
             warp_tot[i] = acc;
             acc += v;
@@ -149,103 +198,65 @@ __global__ void __launch_bounds__(256) recall_kernel(RecallArgs a)
     }
     __syncthreads();
     int pos = warp_tot[warp] + x - mine;
-    int32_t *out = w.cand_idx + (size_t)bh * w.cand_stride;
     for (int i = w0; i < w1; ++i) {
         uint32_t bits = bitmap[i];
         while (bits) {
             const int bit = __ffs(bits) - 1;
-            out[pos++] = (i << 5) + bit;
+            cand_s[pos++] = (i << 5) + bit;
             bits &= bits - 1;
         }
     }
-    if (tid == 0)
-        w.M[bh] = warp_tot[8];
-}
-
-cudaError_t launch_recall(const Work &w, const uint16_t *q, const int32_t *seqlens, cudaStream_t st)
-{
-    RecallArgs a{w, q, seqlens};
-    const size_t smem = (size_t)((w.max_len + 31) / 32) * 4;
-    recall_kernel<<<w.B * w.Hq, 256, smem, st>>>(a);
-    return cudaGetLastError();
-}
-
-// ---------------------------------------------------------------------------
-struct RerankArgs {
-    const int32_t *path;
-    const int32_t *M;
-    const int32_t *cand_idx;
-    uint32_t *cand_key;
-    const uint16_t *q;
-    const uint16_t *k;
-    const int32_t *seqlens;
-    int Hq, Hkv, G, max_len, cand_stride, n_split;
-    float scale;
-};
-
-__global__ void __launch_bounds__(256) rerank_kernel(RerankArgs a)
-{
-    const int bh = blockIdx.y, split = blockIdx.x, tid = threadIdx.x;
-    if (a.path[bh] != RETOPK_PATH_REUSE)
-        return;
-    const int b = bh / a.Hq, hk = (bh % a.Hq) / a.G;
-    const int M = a.M[bh];
-    const int per = (M + a.n_split - 1) / a.n_split;
+    __syncthreads();
+    const int M = warp_tot[8];
+    int32_t *ci = w.cand_idx + (size_t)bh * w.cand_stride;
+    if (split == 0) {
+        for (int j = tid; j < M; j += kRecallThreads)
+            ci[j] = cand_s[j];
+        if (tid == 0)
+            w.M[bh] = M;
+    }
+    // Eq. (10): exact scores of this CTA's candidate slice, half a warp per key
+    // row, kRerankRows rows in flight per half-warp
+    const int per = (M + gridDim.x - 1) / gridDim.x;
     const int start = split * per, end = min(M, start + per);
-    if (start >= end)
-        return;
     const int hw = tid >> 4, hl = tid & 15;
-    const uint4 qv = reinterpret_cast<const uint4 *>(a.q + (size_t)bh * kD)[hl];
-    const float q0 = bf16lo(qv.x), q1 = bf16hi(qv.x), q2 = bf16lo(qv.y), q3 = bf16hi(qv.y);
-    const float q4 = bf16lo(qv.z), q5 = bf16hi(qv.z), q6 = bf16lo(qv.w), q7 = bf16hi(qv.w);
-    const uint16_t *kb = a.k + ((size_t)(b * a.Hkv + hk) * a.max_len) * kD;
-    const int32_t *ci = a.cand_idx + (size_t)bh * a.cand_stride;
-    uint32_t *ck = a.cand_key + (size_t)bh * a.cand_stride;
-    for (int j0 = start + hw; j0 < end; j0 += 16 * 4) {
-        uint4 kv[4];
+    const float *qq = qf + hl * 8;
+    const uint16_t *kb = a.k + ((size_t)(b * w.Hkv + hk) * w.max_len) * kD;
+    uint32_t *ck = w.cand_key + (size_t)bh * w.cand_stride;
+    for (int j0 = start + hw; j0 < end; j0 += (kRecallThreads / 16) * kRerankRows) {
+        uint4 kv[kRerankRows];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int j = j0 + u * 16;
-            if (j < end)
-                kv[u] = reinterpret_cast<const uint4 *>(kb + (size_t)ci[j] * kD)[hl];
-            else
-                kv[u] = make_uint4(0u, 0u, 0u, 0u);
+        for (int u = 0; u < kRerankRows; ++u) {
+            const int j = j0 + u * (kRecallThreads / 16);
+            kv[u] = (j < end) ? reinterpret_cast<const uint4 *>(kb + (size_t)cand_s[j] * kD)[hl]
+                              : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            float s = q0 * bf16lo(kv[u].x) + q1 * bf16hi(kv[u].x) + q2 * bf16lo(kv[u].y) +
-                      q3 * bf16hi(kv[u].y) + q4 * bf16lo(kv[u].z) + q5 * bf16hi(kv[u].z) +
-                      q6 * bf16lo(kv[u].w) + q7 * bf16hi(kv[u].w);
+        for (int u = 0; u < kRerankRows; ++u) {
+            float s = qq[0] * bf16lo(kv[u].x) + qq[1] * bf16hi(kv[u].x) + qq[2] * bf16lo(kv[u].y) +
+                      qq[3] * bf16hi(kv[u].y) + qq[4] * bf16lo(kv[u].z) + qq[5] * bf16hi(kv[u].z) +
+                      qq[6] * bf16lo(kv[u].w) + qq[7] * bf16hi(kv[u].w);
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1)
                 s += __shfl_xor_sync(0xffffffffu, s, o);
-            const int j = j0 + u * 16;
+            const int j = j0 + u * (kRecallThreads / 16);
             if (hl == 0 && j < end)
                 ck[j] = f2key(s * a.scale + 0.0f);
         }
     }
 }
 
-cudaError_t launch_rerank(const Work &w, const uint16_t *q, const uint16_t *k_cache,
-                          const int32_t *seqlens, cudaStream_t st)
+static size_t recall_smem_bytes(int max_len, int RKW)
 {
-    RerankArgs a;
-    a.path = w.path;
-    a.M = w.M;
-    a.cand_idx = w.cand_idx;
-    a.cand_key = w.cand_key;
-    a.q = q;
-    a.k = k_cache;
-    a.seqlens = seqlens;
-    a.Hq = w.Hq;
-    a.Hkv = w.Hkv;
-    a.G = w.G;
-    a.max_len = w.max_len;
-    a.cand_stride = w.cand_stride;
-    a.n_split = w.n_rerank;
-    a.scale = 1.0f / sqrtf((float)kD);
+    return (size_t)((max_len + 31) >> 5) * 4 + (size_t)RKW * 4;
+}
+
+cudaError_t launch_recall(const Work &w, const uint16_t *q, const uint16_t *k_cache, const int32_t *seqlens,
+                          cudaStream_t st)
+{
+    RecallArgs a{w, q, k_cache, seqlens, 1.0f / sqrtf((float)kD)};
     dim3 grid(w.n_rerank, w.B * w.Hq);
-    rerank_kernel<<<grid, 256, 0, st>>>(a);
+    recall_kernel<<<grid, kRecallThreads, recall_smem_bytes(w.max_len, w.R * w.K + w.W), st>>>(a);
     return cudaGetLastError();
 }
 
@@ -303,10 +314,12 @@ cudaError_t launch_init_done(const Work &w, cudaStream_t st)
     return cudaGetLastError();
 }
 
-cudaError_t configure_recall(int max_len_words_bytes)
+cudaError_t configure_recall()
 {
-    return cudaFuncSetAttribute(recall_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                max_len_words_bytes);
+    // the largest request: max_len = 2^20 keys and R*K+W = kMaxC*kMaxK/16 candidates
+    return cudaFuncSetAttribute(recall_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
 }
+
+size_t recall_smem_need(int max_len, int RKW) { return recall_smem_bytes(max_len, RKW); }
 
 }  // namespace retopk

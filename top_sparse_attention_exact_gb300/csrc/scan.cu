@@ -2,39 +2,118 @@
 // Setup Eq. (4): e_i = q . k_i / sqrt(d) for every cached key) fused with the
 // first radix digit of the global Top-K (§Motivation Eq. (1)).
 //
-// One CTA streams a contiguous range of K rows of one (sequence, KV head)
-// and scores them against every query head of the GQA group that takes the
-// exact path this step, so each K row leaves HBM once per group.  The grouped
-// product [16 keys x 128] x [128 x 8 heads] is a dense contraction, so it
-// runs on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).
+// Work: every (sequence, KV head) group that has at least one query head on
+// the exact path this step contributes ceil(L_b / 128) tiles of 128 key rows.
+// The tiles of all active groups are split evenly over a persistent grid of
+// one CTA per SM, so a step with a single exact group still streams with the
+// whole GPU.  Each K row leaves HBM once per group and is scored against
+// every exact query head of the group.
 //
-// Loads go straight from global memory into the A fragments.  The
-// contraction dimension is permuted identically for A (keys) and B (queries)
-// so that each thread's fragment elements of a key row are contiguous: lane
-// (g, t) holds bytes [j*64 + t*16, +16) of rows g and g+8 for j = 0..3, which
-// makes every warp load eight fully used 64-byte row segments (no shared
-// memory staging, no bank conflicts).  In k-step s the logical columns
-// {2t, 2t+1, 2t+8, 2t+9} map to physical elements
-// (s>>1)*32 + t*8 + (s&1)*4 + {0,1,2,3}.
+// Pipeline (per CTA): one producer thread issues one 2-D tensor copy (TMA)
+// per tile -- 256 half rows of 128 bytes, a contiguous 32 KiB block -- into a
+// ring of shared-memory stages, with the 128-byte swizzle and an evict-first
+// L2 policy; eight
+// consumer warps wait on the stage's mbarrier, read their 16 rows as mma
+// A fragments (conflict-free thanks to the swizzle), multiply them with the
+// group's queries on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
+// accumulate) and release the stage.  Every wait is bounded: on expiry the
+// kernel sets RETOPK_STATUS_TIMEOUT, drains its copies and returns.
 //
-// Epilogue: scores (fp32) are written to the workspace, and an 11-bit
-// histogram of their order-preserving keys is accumulated per head in shared
-// memory and flushed with one global atomic per non-empty bin.
+// Fragment layout: the contraction dimension is permuted identically for A
+// (keys) and B (queries) so that each thread's fragment elements of a row
+// form whole 16-byte chunks: lane (g, t) holds chunks 4j+t (j = 0..3) of
+// rows g and g+8; in k-step s the logical columns {2t, 2t+1, 2t+8, 2t+9}
+// are the physical elements (s>>1)*32 + t*8 + (s&1)*4 + {0,1,2,3}.
+//
+// Epilogue: fp32 scores go to the workspace, and an 11-bit histogram of
+// their order-preserving keys is kept per exact head in shared memory and
+// flushed to global memory (one atomic per non-empty bin) when the CTA
+// leaves a group.
+#include <cuda.h>
+
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace retopk {
 
+constexpr int kTileRows = 128;
+constexpr int kStageBytes = kTileRows * kD * 2;          // 32 KiB
+constexpr int kConsumerWarps = 8;
+constexpr int kScanThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxGroups = kMaxSeqGroups;                // B * Hkv
+constexpr long long kWaitCycles = 4000000000LL;          // ~2 s at 2 GHz
+
 struct ScanArgs {
     const uint16_t *q;
     long long q_b_stride, q_h_stride;
-    const uint16_t *k;
     const int32_t *seqlens;
     const int32_t *path;
     float *scores;
     uint32_t *hist;
-    int Hq, Hkv, G, max_len, n_split, len_off;
+    uint32_t *status;
+    int B, Hq, Hkv, G, max_len, sc_stride, len_off, stages;
     float scale;
 };
+
+// ---- PTX helpers ----------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait; returns false (and flags the status word) on expiry.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kWaitCycles) {
+            atomicOr(status, RETOPK_STATUS_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
+                                            uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)),
+          "l"(policy)
+        : "memory");
+}
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                uint32_t a3, uint32_t b0, uint32_t b1)
@@ -46,154 +125,334 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int NT>
-__global__ void __launch_bounds__(256) scan_kernel(ScanArgs a)
+__device__ __forceinline__ void consumer_sync()
 {
-    extern __shared__ uint32_t hist_s[];   // [G][kHistBins]
-    const int b = blockIdx.z, hk = blockIdx.y, split = blockIdx.x;
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+// Fragment row g reads tile row row_perm(g) (and +8): g = 0..7 -> 0 2 1 3 4 6 5 7.
+// The two fragment rows of a quarter warp (g = 2p, 2p+1) then map to half rows
+// whose swizzle phases differ by 4, so every 128-bit shared load is free of
+// bank conflicts.
+__device__ __forceinline__ int row_perm(int g) { return (g & 4) | ((g & 1) << 1) | ((g >> 1) & 1); }
+
+struct ScanShared {
+    uint64_t full[8];
+    uint64_t empty[8];
+    int n_groups;
+    int total_tiles;
+    int grp_first[kMaxGroups + 1];  // prefix of tiles over groups b * Hkv + hk
+    uint32_t grp_mask[kMaxGroups];
+};
+
+template <int NT>
+__global__ void __launch_bounds__(kScanThreads, 1)
+    scan_kernel(const __grid_constant__ CUtensorMap kmap, const ScanArgs a)
+{
+    extern __shared__ __align__(1024) unsigned char scan_smem[];
+    __shared__ ScanShared sh;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, t = lane & 3;
     const int G = a.G;
+    const int S = a.stages;
+    unsigned char *ring = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(scan_smem) + 1023) & ~uintptr_t(1023));
+    uint32_t *hist_s = reinterpret_cast<uint32_t *>(ring + (size_t)S * kStageBytes);   // [G][kHistBins]
 
-    uint32_t mask = 0;
-    for (int n = 0; n < G; ++n)
-        if (!a.path || a.path[b * a.Hq + hk * G + n] != 0)
-            mask |= 1u << n;
-    if (!mask)
-        return;
-
-    const int L = seq_len(a.seqlens, b, a.len_off, a.max_len);
-    const int chunk = (((L + a.n_split - 1) / a.n_split) + 15) & ~15;
-    const int start = split * chunk;
-    const int end = min(L, start + chunk);
-    if (start >= end)
-        return;
-
-    for (int i = tid; i < G * kHistBins; i += blockDim.x)
-        if ((mask >> (i / kHistBins)) & 1u)
-            hist_s[i] = 0;
-
-    // B fragments: query head n = nt*8 + g of the group, same column permutation
-    uint4 qf[NT][4];
+    // ---- active groups and their tile ranges (every CTA computes the same
+    //      list): groups with no exact head get zero tiles
+    const int NG = a.B * a.Hkv;
+    for (int i = tid; i < NG; i += kScanThreads) {
+        const int b = i / a.Hkv, hk = i % a.Hkv;
+        uint32_t mask = 0;
+        if (!a.path) {
+            mask = (G >= 32) ? 0xffffffffu : ((1u << G) - 1u);
+        } else {
+            const int32_t *pp = a.path + b * a.Hq + hk * G;
+            for (int j = 0; j < G; ++j)
+                mask |= (pp[j] != 0 ? 1u : 0u) << j;
+        }
+        const int L = seq_len(a.seqlens, b, a.len_off, a.max_len);
+        sh.grp_mask[i] = mask;
+        sh.grp_first[i + 1] = (mask && L > 0) ? (L + kTileRows - 1) / kTileRows : 0;
+    }
+    if (tid == 0) {
+        sh.grp_first[0] = 0;
+        for (int s2 = 0; s2 < S; ++s2) {
+            mbar_init(&sh.full[s2], 1);
+            mbar_init(&sh.empty[s2], kConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    // inclusive prefix over the per-group tile counts (one warp, NG <= 512)
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 1; base <= NG; base += 32) {
+            const int i = base + lane;
+            int v = (i <= NG) ? sh.grp_first[i] : 0;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int n = nt * 8 + g;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (n < G) {
-                const uint4 *qp = reinterpret_cast<const uint4 *>(
-                    a.q + b * a.q_b_stride + (long long)(hk * G + n) * a.q_h_stride);
-                qf[nt][j] = qp[j * 4 + t];
-            } else {
-                qf[nt][j] = make_uint4(0u, 0u, 0u, 0u);
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o)
+                    v += y;
             }
+            if (i <= NG)
+                sh.grp_first[i] = v + carry;
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (lane == 0) {
+            sh.n_groups = NG;
+            sh.total_tiles = carry;
         }
     }
     __syncthreads();
+    const int T = sh.total_tiles;
+    const int t_begin = (int)(((long long)T * blockIdx.x) / gridDim.x);
+    const int t_end = (int)(((long long)T * (blockIdx.x + 1)) / gridDim.x);
 
-    const uint16_t *kb = a.k + ((size_t)(b * a.Hkv + hk) * a.max_len) * kD;
-    float *sc_base = a.scores + (size_t)(b * a.Hq + hk * G) * a.max_len;
-
-    for (int tile = start + warp * 16; tile < end; tile += 8 * 16) {
-        const int r0 = tile + g, r1 = tile + g + 8;
-        const int l0 = min(r0, end - 1), l1 = min(r1, end - 1);
-        const uint4 *p0 = reinterpret_cast<const uint4 *>(kb + (size_t)l0 * kD);
-        const uint4 *p1 = reinterpret_cast<const uint4 *>(kb + (size_t)l1 * kD);
-        uint4 x0[4], x1[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            x0[j] = ld_stream(p0 + j * 4 + t);
-            x1[j] = ld_stream(p1 + j * 4 + t);
-        }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const int j = s >> 1;
-                const bool hi = s & 1;
-                const uint32_t a0 = hi ? x0[j].z : x0[j].x;
-                const uint32_t a2 = hi ? x0[j].w : x0[j].y;
-                const uint32_t a1 = hi ? x1[j].z : x1[j].x;
-                const uint32_t a3 = hi ? x1[j].w : x1[j].y;
-                const uint32_t b0 = hi ? qf[nt][j].z : qf[nt][j].x;
-                const uint32_t b1 = hi ? qf[nt][j].w : qf[nt][j].y;
-                mma_bf16_16816(c, a0, a1, a2, a3, b0, b1);
+    if (warp == kConsumerWarps) {
+        // ================= producer =================
+        if (lane == 0 && t_begin < t_end) {
+            uint64_t policy;
+            asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+            int gi = 0;
+            bool ok = true;
+            for (int it = 0, tile = t_begin; tile < t_end && ok; ++it, ++tile) {
+                while (tile >= sh.grp_first[gi + 1])
+                    ++gi;
+                const int s = it % S;
+                if (it >= S)
+                    ok = mbar_wait(&sh.empty[s], ((it / S) - 1) & 1, a.status);
+                if (!ok)
+                    break;
+                const int row = gi * a.max_len + (tile - sh.grp_first[gi]) * kTileRows;
+                unsigned char *dst = ring + (size_t)s * kStageBytes;
+                mbar_expect_tx(&sh.full[s], kStageBytes);
+                tma_load_2d(dst, &kmap, 0, 2 * row, &sh.full[s], policy);
             }
-            // c[0]: (row r0, head 2t)  c[1]: (r0, 2t+1)  c[2]: (r1, 2t)  c[3]: (r1, 2t+1)
+        }
+    } else {
+        // ================= consumers =================
+        const int g = lane >> 2, t = lane & 3;
+        int gi = -1;
+        uint32_t mask = 0;
+        int b = 0, hk = 0, L = 0;
+        uint4 qf[NT][4];
+        bool ok = true;
+        for (int it = 0, tile = t_begin; tile < t_end; ++it, ++tile) {
+            int ng = gi < 0 ? 0 : gi;
+            while (tile >= sh.grp_first[ng + 1])
+                ++ng;
+            if (ng != gi) {
+                consumer_sync();
+                if (gi >= 0) {   // flush the previous group's histogram
+                    uint32_t *hg = a.hist + (size_t)(b * a.Hq + hk * G) * kHistBins;
+                    for (int i = tid; i < G * kHistBins; i += kConsumerWarps * 32)
+                        if ((mask >> (i / kHistBins)) & 1u) {
+                            const uint32_t v = hist_s[i];
+                            if (v)
+                                atomicAdd(&hg[i], v);
+                        }
+                    consumer_sync();
+                }
+                gi = ng;
+                mask = sh.grp_mask[gi];
+                b = gi / a.Hkv;
+                hk = gi % a.Hkv;
+                L = seq_len(a.seqlens, b, a.len_off, a.max_len);
+                for (int i = tid; i < G * kHistBins; i += kConsumerWarps * 32)
+                    if ((mask >> (i / kHistBins)) & 1u)
+                        hist_s[i] = 0u;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int n = nt * 8 + 2 * t + (e & 1);
-                const int r = (e < 2) ? r0 : r1;
-                if (n < G && r < end && ((mask >> n) & 1u)) {
-                    const float sc = c[e] * a.scale + 0.0f;
-                    sc_base[(size_t)n * a.max_len + r] = sc;
-                    atomicAdd(&hist_s[n * kHistBins + (f2key(sc) >> (32 - kHistBits))], 1u);
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int n = nt * 8 + g;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (n < G) {
+                            const uint4 *qp = reinterpret_cast<const uint4 *>(
+                                a.q + b * a.q_b_stride + (long long)(hk * G + n) * a.q_h_stride);
+                            qf[nt][j] = qp[j * 4 + t];
+                        } else {
+                            qf[nt][j] = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                }
+                consumer_sync();
+            }
+            const int s = it % S;
+            if (ok)
+                ok = mbar_wait(&sh.full[s], (it / S) & 1, a.status);
+            if (!ok)
+                continue;   // keep walking the tiles so the named barriers still match
+            const unsigned char *st = ring + (size_t)s * kStageBytes;
+            const int base = (tile - sh.grp_first[gi]) * kTileRows;   // first row of the tile
+            const int rl0 = warp * 16 + row_perm(g), rl1 = rl0 + 8;    // rows within the tile
+            uint4 x0[4], x1[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                // half row h = j>>1 of key row r is box row 2r+h; its 16-byte
+                // chunk cc sits at position cc ^ ((2r+h) & 7)
+                const int hr0 = 2 * rl0 + (j >> 1), hr1 = 2 * rl1 + (j >> 1), cc = ((j & 1) << 2) + t;
+                x0[j] = *reinterpret_cast<const uint4 *>(st + hr0 * 128 + ((cc ^ (hr0 & 7)) << 4));
+                x1[j] = *reinterpret_cast<const uint4 *>(st + hr1 * 128 + ((cc ^ (hr1 & 7)) << 4));
+            }
+            const int r0 = base + rl0, r1 = base + rl1;
+            float *sc_base = a.scores + (size_t)(b * a.Hq + hk * G) * a.sc_stride;
+            float c[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int j = ks >> 1;
+                    const bool hi = ks & 1;
+                    mma_bf16_16816(c[nt], hi ? x0[j].z : x0[j].x, hi ? x1[j].z : x1[j].x,
+                                   hi ? x0[j].w : x0[j].y, hi ? x1[j].w : x1[j].y, hi ? qf[nt][j].z : qf[nt][j].x,
+                                   hi ? qf[nt][j].w : qf[nt][j].y);
+                }
+            }
+            // the stage's rows have been consumed by the MMAs: hand it back
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sh.empty[s]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                // c[0]: (row r0, head 2t)  c[1]: (r0, 2t+1)  c[2]: (r1, 2t)  c[3]: (r1, 2t+1)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int n = nt * 8 + 2 * t + (e & 1);
+                    const int r = (e < 2) ? r0 : r1;
+                    if (n < G && r < L && ((mask >> n) & 1u)) {
+                        const float sc = c[nt][e] * a.scale + 0.0f;
+                        sc_base[(size_t)n * a.sc_stride + r] = sc;
+                        atomicAdd(&hist_s[n * kHistBins + (f2key(sc) >> (32 - kHistBits))], 1u);
+                    }
                 }
             }
         }
+        consumer_sync();
+        if (gi >= 0) {
+            uint32_t *hg = a.hist + (size_t)(b * a.Hq + hk * G) * kHistBins;
+            for (int i = tid; i < G * kHistBins; i += kConsumerWarps * 32)
+                if ((mask >> (i / kHistBins)) & 1u) {
+                    const uint32_t v = hist_s[i];
+                    if (v)
+                        atomicAdd(&hg[i], v);
+                }
+        }
     }
     __syncthreads();
-    uint32_t *hg = a.hist + (size_t)(b * a.Hq + hk * G) * kHistBins;
-    for (int i = tid; i < G * kHistBins; i += blockDim.x) {
-        if ((mask >> (i / kHistBins)) & 1u) {
-            const uint32_t v = hist_s[i];
-            if (v)
-                atomicAdd(&hg[i], v);
+    // Drain: every issued copy has landed before shared memory is released
+    // (immediate on the normal path, where the consumers waited on each one).
+    if (tid == kConsumerWarps * 32) {
+        const int n = t_end - t_begin;
+        for (int s = 0; s < S && s < n; ++s) {
+            const int last = s + ((n - 1 - s) / S) * S;     // last issue index that used stage s
+            mbar_wait(&sh.full[s], (last / S) & 1, a.status);
         }
     }
 }
 
-static size_t scan_smem(int G) { return (size_t)G * kHistBins * sizeof(uint32_t); }
+// ---- host side --------------------------------------------------------------
+static size_t hist_bytes(int G) { return (size_t)G * kHistBins * sizeof(uint32_t); }
 
-int scan_ctas_per_sm()
+static int stages_for(int G)
 {
-    static int cached = 0;
-    if (!cached) {
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, scan_kernel<1>, 256, scan_smem(8)) != cudaSuccess || n < 1)
-            n = 1;
-        cached = n;
+    const size_t budget = 227 * 1024 - sizeof(ScanShared) - 1024 - hist_bytes(G);
+    int s = (int)(budget / kStageBytes);
+    return s > 6 ? 6 : (s < 2 ? 2 : s);
+}
+
+static size_t scan_smem_bytes(int G) { return 1024 + (size_t)stages_for(G) * kStageBytes + hist_bytes(G); }
+
+int scan_ctas_per_sm() { return 1; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
     }
-    return cached;
+    return fn;
+}
+
+// K cache viewed as a 2-D tensor of 128-byte half rows: [2*B*Hkv*max_len, 64
+// elements].  One box of 256 half rows is one contiguous 32 KiB tile.
+static cudaError_t make_kmap(CUtensorMap *map, const uint16_t *k, int B, int Hkv, int max_len)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)kD / 2, (cuuint64_t)2 * B * Hkv * max_len};
+    cuuint64_t strides[1] = {(cuuint64_t)kD};            // 128 bytes per half row
+    cuuint32_t box[2] = {64, 2 * kTileRows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(k), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 cudaError_t launch_scan(const Work &w, QSrc q, const uint16_t *k_cache, const int32_t *seqlens,
-                        int len_off, cudaStream_t st)
+                        int len_off, cudaStream_t st, cudaEvent_t ev0, cudaEvent_t ev1)
 {
+    if ((size_t)w.B * w.Hkv > (size_t)kMaxGroups)
+        return cudaErrorInvalidValue;
+    CUtensorMap map;
+    cudaError_t e = make_kmap(&map, k_cache, w.B, w.Hkv, w.max_len);
+    if (e != cudaSuccess)
+        return e;
     ScanArgs a;
     a.q = q.q;
     a.q_b_stride = q.b_stride;
     a.q_h_stride = q.h_stride;
-    a.k = k_cache;
     a.seqlens = seqlens;
     a.path = w.path;
     a.scores = w.scores;
     a.hist = w.hist;
+    a.status = w.status;
+    a.B = w.B;
     a.Hq = w.Hq;
     a.Hkv = w.Hkv;
     a.G = w.G;
     a.max_len = w.max_len;
-    a.n_split = w.n_scan;
+    a.sc_stride = w.sc_stride;
     a.len_off = len_off;
+    a.stages = stages_for(w.G);
     a.scale = 1.0f / sqrtf((float)kD);
-    dim3 grid(w.n_scan, w.Hkv, w.B);
-    const size_t smem = scan_smem(w.G);
+    const size_t smem = scan_smem_bytes(w.G);
+    if (ev0)
+        cudaEventRecord(ev0, st);
     if (w.G <= 8)
-        scan_kernel<1><<<grid, 256, smem, st>>>(a);
+        scan_kernel<1><<<w.n_scan, kScanThreads, smem, st>>>(map, a);
     else
-        scan_kernel<2><<<grid, 256, smem, st>>>(a);
-    return cudaGetLastError();
+        scan_kernel<2><<<w.n_scan, kScanThreads, smem, st>>>(map, a);
+    e = cudaGetLastError();
+    if (ev1)
+        cudaEventRecord(ev1, st);
+    return e;
 }
 
 cudaError_t configure_scan()
 {
-    cudaError_t e = cudaFuncSetAttribute(scan_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)scan_smem(8));
+    size_t m1 = 0, m2 = 0;   // the largest request of each instantiation
+    for (int G = 1; G <= kMaxGroup; ++G)
+        (G <= 8 ? m1 : m2) = std::max(G <= 8 ? m1 : m2, scan_smem_bytes(G));
+    cudaError_t e = cudaFuncSetAttribute(scan_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m1);
     if (e != cudaSuccess)
         return e;
-    return cudaFuncSetAttribute(scan_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)scan_smem(kMaxGroup));
+    return cudaFuncSetAttribute(scan_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m2);
 }
 
 }  // namespace retopk

@@ -24,7 +24,7 @@ STATUS_BAD_INDEX, STATUS_KV_FULL, STATUS_NONFINITE = 0x1, 0x2, 0x4
 EXPORTED = ("retopk_workspace_bytes", "retopk_create", "retopk_destroy", "retopk_init_cache",
             "retopk_append_kv", "retopk_decode_step", "retopk_get_diagnostics",
             "retopk_get_counters", "retopk_state_bytes", "retopk_export_state",
-            "retopk_import_state", "retopk_get_status", "retopk_strerror",
+            "retopk_import_state", "retopk_get_status", "retopk_strerror", "retopk_cuda_error_string",
             "exact_topk_workspace_bytes", "exact_topk_attention_step",
             "retopk_profile_enable", "retopk_profile_read")
 
@@ -62,6 +62,8 @@ def _declare(lib):
     lib.retopk_get_status.argtypes = [_P, _P, _I, _P]
     lib.retopk_strerror.argtypes = [_I]
     lib.retopk_strerror.restype = ctypes.c_char_p
+    lib.retopk_cuda_error_string.argtypes = []
+    lib.retopk_cuda_error_string.restype = ctypes.c_char_p
     lib.exact_topk_workspace_bytes.argtypes = [_I] * 6
     lib.exact_topk_workspace_bytes.restype = _S
     lib.exact_topk_attention_step.argtypes = [_P, _P, _P, _P] + [_I] * 6 + [_P, _P, _P, _S, _P]
@@ -90,6 +92,8 @@ def load(build: bool = True):
 def _check(rc: int, what: str):
     if rc != 0:
         msg = load().retopk_strerror(rc).decode()
+        if rc == -4:
+            msg += ": " + load().retopk_cuda_error_string().decode()
         raise RetopkError(f"{what} failed: {msg} ({rc})")
 
 
