@@ -13,7 +13,7 @@
 namespace retopk {
 cudaError_t configure_scan();
 cudaError_t configure_select();
-cudaError_t configure_recall();
+cudaError_t configure_reuse();
 }  // namespace retopk
 
 using namespace retopk;
@@ -75,7 +75,7 @@ int ensure_configured()
         if (err == cudaSuccess)
             err = configure_select();
         if (err == cudaSuccess)
-            err = configure_recall();
+            err = configure_reuse();
     });
     return cuda_rc(err);
 }
@@ -110,7 +110,6 @@ size_t plan(const retopk_config &c, bool stateful, Work *w, char *base)
     x.n_filter = n_filter_for(c.max_len);
     const int RKW = stateful ? c.R * c.K + c.W : 0;
     x.cand_stride = cand_stride_for(c.max_len, x.n_filter, RKW);
-    x.n_rerank = stateful ? std::min(32, std::max(1, (RKW + 255) / 256)) : 1;
     x.sc_stride = (c.max_len + 15) & ~15;
     const size_t BH = (size_t)c.batch * c.n_q_heads;
     Layout L;
@@ -334,7 +333,7 @@ int retopk_decode_step(retopk_ctx *ctx, const retopk_bf16 *q, const retopk_bf16 
     const Work &w = ctx->w;
     QSrc qs{q, (long long)w.Hq * kD, kD};
     int e;
-    if ((e = cuda_rc(launch_recall(w, q, k_cache, d_seqlens, st))))
+    if ((e = cuda_rc(launch_reuse(w, q, k_cache, v_cache, d_seqlens, out, st))))
         return e;
     if ((e = run_scan(w, qs, k_cache, d_seqlens, 0, st)))
         return e;

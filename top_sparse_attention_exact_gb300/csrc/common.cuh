@@ -34,7 +34,6 @@ struct Work {
     int cand_stride;   // per-head capacity of cand_idx / cand_key
     int n_filter;      // filter CTAs (segments) per head
     int n_scan;        // scan CTAs per (b, h_kv)
-    int n_rerank;      // recall/rerank CTAs per head
     int sc_stride;     // row stride of `scores` (max_len rounded up to 16)
     // query-support cache (decode contexts only)
     uint16_t *fifo_q;
@@ -92,6 +91,14 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
+__device__ __forceinline__ int warp_isum(int v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
 // Effective length of sequence b for a launch (len_off < 0 during cache
 // initialisation, where the causal prefix of a prompt position is scored).
 // Clamped to the cache capacity so that a bad length can never index past it.
@@ -115,8 +122,8 @@ cudaError_t launch_filter(const Work &w, const int32_t *seqlens, int len_off, cu
 cudaError_t launch_finalize(const Work &w, QSrc q, const uint16_t *v_cache, const int32_t *seqlens,
                             int len_off, int mode, int init_slot, uint16_t *out, int32_t *idx_out,
                             cudaStream_t st);
-cudaError_t launch_recall(const Work &w, const uint16_t *q, const uint16_t *k_cache, const int32_t *seqlens,
-                          cudaStream_t st);
+cudaError_t launch_reuse(const Work &w, const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                         const int32_t *seqlens, uint16_t *out, cudaStream_t st);
 cudaError_t launch_append(const Work &w, const uint16_t *k_new, const uint16_t *v_new,
                           uint16_t *k_cache, uint16_t *v_cache, int32_t *seqlens, cudaStream_t st);
 cudaError_t launch_init_done(const Work &w, cudaStream_t st);

@@ -7,8 +7,8 @@
 //                    score, and compacts every key whose digit is >= it, in
 //                    ascending index order, one segment per CTA.  Only these
 //                    keys can belong to the Exact Top-K support (Eq. (1)).
-//   finalize_kernel  per (sequence, query head): exact Top-K (Eq. (1) or
-//                    Eq. (11)) over the candidate list by radix select on a
+//   finalize_kernel  per exact-path (sequence, query head): Top-K (Eq. (1))
+//                    over the filter's candidate list by radix select on a
 //                    64-bit key (score, then lower index), stable compaction
 //                    so the support comes out in ascending index order,
 //                    softmax over its scores and the weighted sum of the V
@@ -19,46 +19,9 @@
 // Both kernels are latency-bound at batch 1, so every thread issues all of its
 // global loads before it consumes any of them, and the number of block-wide
 // barriers is kept small.
-#include "common.cuh"
+#include "topk.cuh"
 
 namespace retopk {
-
-// ---------------------------------------------------------------------------
-// Block-wide exclusive scan of one int per thread (NT threads, NT % 32 == 0).
-template <int NT>
-__device__ __forceinline__ int block_excl_scan(int v, int *warp_tot, int &total)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o)
-            x += y;
-    }
-    if (lane == 31)
-        warp_tot[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        const int w = lane < NT / 32 ? warp_tot[lane] : 0;
-        int s = w;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o)
-                s += y;
-        }
-        if (lane < NT / 32)
-            warp_tot[lane] = s - w;
-        if (lane == NT / 32 - 1)
-            warp_tot[32] = s;
-    }
-    __syncthreads();
-    const int r = warp_tot[warp] + x - v;
-    total = warp_tot[32];
-    __syncthreads();
-    return r;
-}
 
 // ---------------------------------------------------------------------------
 struct FilterArgs {
@@ -72,12 +35,13 @@ struct FilterArgs {
     int Hq, max_len, sc_stride, K, n_filter, cand_stride, len_off;
 };
 
-constexpr int kFilterThreads = 512;
-constexpr int kFilterPer = 16;                       // scores per thread per chunk
+constexpr int kFilterThreads = 256;
+constexpr int kFilterPer = 32;                       // scores per thread per chunk
 
 __global__ void __launch_bounds__(kFilterThreads) filter_kernel(FilterArgs a)
 {
     __shared__ int warp_tot[33];
+    __shared__ __align__(16) uint32_t hist_s[kHistBins];   // filled with 16-byte stores
     __shared__ int T1_s;
     const int bh = blockIdx.y, s = blockIdx.x, tid = threadIdx.x;
     const int b = bh / a.Hq;
@@ -85,41 +49,13 @@ __global__ void __launch_bounds__(kFilterThreads) filter_kernel(FilterArgs a)
         return;
     const int L = seq_len(a.seqlens, b, a.len_off, a.max_len);
     const int need = min(a.K, L);
-
-    // threshold digit T1: the largest digit whose suffix count reaches `need`
-    constexpr int per = kHistBins / kFilterThreads;   // 4 bins per thread
-    static_assert(per == 4, "one uint4 of bins per thread");
-    const uint4 hv = reinterpret_cast<const uint4 *>(a.hist + (size_t)bh * kHistBins)[tid];
-    const int part = (int)(hv.x + hv.y + hv.z + hv.w);
-    if (tid == 0)
-        T1_s = 0;
-    int tot;
-    const int below = block_excl_scan<kFilterThreads>(part, warp_tot, tot);   // bins under mine
-    const int above = tot - below - part;                                      // bins over mine
-    if (need > 0 && above < need && above + part >= need) {
-        int acc = above;
-        const uint32_t hb[4] = {hv.x, hv.y, hv.z, hv.w};
-        for (int i = per - 1; i >= 0; --i) {
-            acc += (int)hb[i];
-            if (acc >= need) {
-                T1_s = tid * per + i;
-                break;
-            }
-        }
-    }
-    __syncthreads();
-    const uint32_t T1 = (uint32_t)T1_s;
-
     const int seg = (((L + a.n_filter - 1) / a.n_filter) + 15) & ~15;
     const int start = s * seg;
     const int end = min(L, start + seg);
     const float *sc = a.scores + (size_t)bh * a.sc_stride;
-    int32_t *oi = a.cand_idx + (size_t)bh * a.cand_stride + start;
-    uint32_t *ok = a.cand_key + (size_t)bh * a.cand_stride + start;
-    int count = 0;
-    for (int chunk = start; chunk < end; chunk += kFilterThreads * kFilterPer) {   // uniform trip count
-        const int i0 = chunk + tid * kFilterPer;
-        uint32_t key[kFilterPer];
+
+    // issue the first chunk's score loads and the histogram loads together
+    auto load_chunk = [&](int i0, uint32_t (&key)[kFilterPer]) {
         if (i0 + kFilterPer <= end) {
 #pragma unroll
             for (int v = 0; v < kFilterPer / 4; ++v) {
@@ -134,6 +70,52 @@ __global__ void __launch_bounds__(kFilterThreads) filter_kernel(FilterArgs a)
             for (int e = 0; e < kFilterPer; ++e)
                 key[e] = (i0 + e < end) ? f2key(sc[i0 + e]) : 0u;
         }
+    };
+    uint32_t key[kFilterPer];
+    load_chunk(start + tid * kFilterPer, key);
+    {
+        const uint4 *hg = reinterpret_cast<const uint4 *>(a.hist + (size_t)bh * kHistBins);
+        uint4 hv[kHistBins / 4 / kFilterThreads];
+#pragma unroll
+        for (int u = 0; u < kHistBins / 4 / kFilterThreads; ++u)
+            hv[u] = hg[tid + u * kFilterThreads];
+#pragma unroll
+        for (int u = 0; u < kHistBins / 4 / kFilterThreads; ++u)
+            reinterpret_cast<uint4 *>(hist_s)[tid + u * kFilterThreads] = hv[u];
+    }
+    if (tid == 0)
+        T1_s = 0;
+    __syncthreads();
+    // threshold digit T1: the largest digit whose suffix count reaches `need`;
+    // thread t owns the 8 digits [8t, 8t+8)
+    constexpr int per = kHistBins / kFilterThreads;
+    int part = 0;
+#pragma unroll
+    for (int i = 0; i < per; ++i)
+        part += (int)hist_s[tid * per + i];
+    int tot;
+    const int below = block_excl_scan<kFilterThreads>(part, warp_tot, tot);
+    const int above = tot - below - part;
+    if (need > 0 && above < need && above + part >= need) {
+        int acc = above;
+        for (int i = per - 1; i >= 0; --i) {
+            acc += (int)hist_s[tid * per + i];
+            if (acc >= need) {
+                T1_s = tid * per + i;
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    const uint32_t T1 = (uint32_t)T1_s;
+
+    int32_t *oi = a.cand_idx + (size_t)bh * a.cand_stride + start;
+    uint32_t *ok = a.cand_key + (size_t)bh * a.cand_stride + start;
+    int count = 0;
+    for (int chunk = start; chunk < end; chunk += kFilterThreads * kFilterPer) {   // uniform trip count
+        const int i0 = chunk + tid * kFilterPer;
+        if (chunk != start)
+            load_chunk(i0, key);
         int n = 0;
 #pragma unroll
         for (int e = 0; e < kFilterPer; ++e)
@@ -193,9 +175,7 @@ constexpr int kFinWarps = kFinThreads / 32;
 
 struct FinShared {
     int seg_off[kMaxSeg + 1];
-    int warp_tot[33];
-    uint32_t hist[2][256];
-    int digit, above, cnt_d;
+    SelectShared sel;
     uint32_t kmax;
     float Z_w[kFinWarps];
     int slot;
@@ -244,6 +224,8 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinArgs a)
     const int b = bh / w.Hq, h = bh % w.Hq, hk = h / w.G;
     const int L = seq_len(a.seqlens, b, a.len_off, w.max_len);
     const int path = (a.mode == FIN_DECODE) ? w.path[bh] : RETOPK_PATH_FALLBACK;
+    if (path == RETOPK_PATH_REUSE)
+        return;   // the reuse kernel has served this head
 
     int32_t *st_idx = reinterpret_cast<int32_t *>(fin_smem);                  // [kStageCap]
     uint32_t *st_key = reinterpret_cast<uint32_t *>(st_idx + kStageCap);      // [kStageCap]
@@ -252,35 +234,25 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinArgs a)
     uint32_t *sup_k = reinterpret_cast<uint32_t *>(sup_i + Kp);               // [Kp]
     float *red = reinterpret_cast<float *>(sup_k + Kp);                       // [kFinWarps][kD]
 
-    // ---- candidate segments (reuse: one list of M_t; exact: filter segments)
-    int nseg, seg;
-    if (path == RETOPK_PATH_REUSE) {
-        nseg = 1;
-        seg = 0;
-        if (tid == 0) {
-            sh.seg_off[0] = 0;
-            sh.seg_off[1] = w.M[bh];
-        }
-    } else {
-        nseg = w.n_filter;
-        seg = (((L + w.n_filter - 1) / w.n_filter) + 15) & ~15;
-        if (warp == 0) {
-            // nseg <= 64: two counts per lane, warp-wide inclusive scan
-            const int c0 = (2 * lane < nseg) ? w.seg_count[(size_t)bh * nseg + 2 * lane] : 0;
-            const int c1 = (2 * lane + 1 < nseg) ? w.seg_count[(size_t)bh * nseg + 2 * lane + 1] : 0;
-            int x = c0 + c1;
+    // ---- candidate segments written by the filter kernel ---------------------
+    const int nseg = w.n_filter;
+    const int seg = (((L + w.n_filter - 1) / w.n_filter) + 15) & ~15;
+    if (warp == 0) {
+        // nseg <= 64: two counts per lane, warp-wide inclusive scan
+        const int c0 = (2 * lane < nseg) ? w.seg_count[(size_t)bh * nseg + 2 * lane] : 0;
+        const int c1 = (2 * lane + 1 < nseg) ? w.seg_count[(size_t)bh * nseg + 2 * lane + 1] : 0;
+        int x = c0 + c1;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o)
-                    x += y;
-            }
-            const int ex = x - c0 - c1;
-            if (2 * lane <= nseg)
-                sh.seg_off[2 * lane] = ex;
-            if (2 * lane + 1 <= nseg)
-                sh.seg_off[2 * lane + 1] = ex + c0;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o)
+                x += y;
         }
+        const int ex = x - c0 - c1;
+        if (2 * lane <= nseg)
+            sh.seg_off[2 * lane] = ex;
+        if (2 * lane + 1 <= nseg)
+            sh.seg_off[2 * lane + 1] = ex + c0;
     }
     __syncthreads();
     const int N = sh.seg_off[nseg];
@@ -296,90 +268,12 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinArgs a)
             st_key[j] = gk[o];
         }
     }
-    for (int i = tid; i < 512; i += kFinThreads)
-        (&sh.hist[0][0])[i] = 0u;
     __syncthreads();
 
-    // ---- radix select of the `need` largest composite keys (8-bit digits) --
-    unsigned long long thr = 0ull;
-    if (N > need) {
-        unsigned long long prefix = 0ull;
-        int rem = need;
-        int buf = 0;
-        for (int shift = 56; shift >= 0; shift -= 8, buf ^= 1) {
-            const unsigned long long hmask = (shift == 56) ? 0ull : (~0ull << (shift + 8));
-            uint32_t *hist = sh.hist[buf];
-            for (int j = tid; j < N; j += kFinThreads) {
-                int32_t idx;
-                uint32_t key;
-                cv.get(j, idx, key);
-                const unsigned long long k64 = key64(key, idx);
-                if (((k64 ^ prefix) & hmask) == 0ull)
-                    atomicAdd(&hist[(k64 >> shift) & 255ull], 1u);
-            }
-            __syncthreads();
-            if (warp == 0) {
-                int c8[8];
-                int t8 = 0;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    c8[i] = (int)hist[lane * 8 + i];
-                    t8 += c8[i];
-                }
-                int sfx = t8;   // inclusive suffix over lanes >= lane
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_down_sync(0xffffffffu, sfx, o);
-                    if (lane + o < 32)
-                        sfx += y;
-                }
-                int above = sfx - t8;
-                if (above < rem && rem <= sfx) {
-                    for (int i = 7; i >= 0; --i) {
-                        if (above + c8[i] >= rem) {
-                            sh.digit = lane * 8 + i;
-                            sh.above = above;
-                            sh.cnt_d = c8[i];
-                            break;
-                        }
-                        above += c8[i];
-                    }
-                }
-            } else if (warp == 1) {
-                // clear the other buffer for the next pass
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    sh.hist[buf ^ 1][lane * 8 + i] = 0u;
-            }
-            __syncthreads();
-            rem -= sh.above;
-            prefix |= (unsigned long long)sh.digit << shift;
-            if (sh.cnt_d == rem)
-                break;                 // every key with this prefix is selected
-        }
-        thr = prefix;
-    }
-
-    // ---- stable compaction: the support in ascending index order -----------
-    int got = 0;
-    for (int base = 0; base < N; base += kFinThreads) {
-        const int j = base + tid;
-        int32_t idx = 0;
-        uint32_t key = 0;
-        int flag = 0;
-        if (j < N) {
-            cv.get(j, idx, key);
-            flag = key64(key, idx) >= thr;
-        }
-        int total;
-        const int pos = block_excl_scan<kFinThreads>(flag, sh.warp_tot, total);
-        if (flag && got + pos < w.K) {
-            sup_i[got + pos] = idx;
-            sup_k[got + pos] = key;
-        }
-        got += total;
-    }
-    const int n = min(got, w.K);
+    // ---- Eq. (1): the K best candidates, ascending index order ---------------
+    auto get = [&](int j, int32_t &idx, uint32_t &key) { cv.get(j, idx, key); };
+    const unsigned long long thr = radix_select_threshold<kFinThreads>(N, need, get, sh.sel);
+    const int n = stable_compact<kFinThreads>(N, thr, get, w.K, sup_i, sup_k, sh.sel.warp_tot);
 
     // ---- softmax over the support and value aggregation (Eq. (12)) --------
     if (tid == 0)
@@ -398,32 +292,8 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinArgs a)
     const uint16_t *vb = a.v + ((size_t)(b * w.Hkv + hk) * w.max_len) * kD;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float zsum = 0.f;
-    if (a.mode != FIN_INIT) {   // cache initialisation needs the support only
-        // warp `warp` owns support rows warp, warp+32, ...; 16 loads in flight per lane
-        for (int j0 = warp; j0 < n; j0 += kFinWarps * 16) {
-            uint2 vv[16];
-            float p[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int j = j0 + u * kFinWarps;
-                if (j < n) {
-                    vv[u] = *reinterpret_cast<const uint2 *>(vb + (size_t)sup_i[j] * kD + lane * 4);
-                    p[u] = expf(key2f(sup_k[j]) - m);
-                } else {
-                    vv[u] = make_uint2(0u, 0u);
-                    p[u] = 0.f;
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                zsum += p[u];
-                acc[0] += p[u] * bf16lo(vv[u].x);
-                acc[1] += p[u] * bf16hi(vv[u].x);
-                acc[2] += p[u] * bf16lo(vv[u].y);
-                acc[3] += p[u] * bf16hi(vv[u].y);
-            }
-        }
-    }
+    if (a.mode != FIN_INIT)   // cache initialisation needs the support only
+        value_partial(vb, sup_i, sup_k, warp, n, kFinWarps, m, acc, zsum);
     *reinterpret_cast<float4 *>(red + warp * kD + lane * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     if (lane == 0)
         sh.Z_w[warp] = zsum;
@@ -465,28 +335,8 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinArgs a)
         if (tid == 0)
             w.fifo_len[e] = n;
     }
-    if (a.mode == FIN_DECODE && tid == 0) {
-        unsigned long long *cnt = w.counters + (size_t)b * CNT_WORDS;
-        atomicAdd(&cnt[path == RETOPK_PATH_REUSE ? CNT_REUSE
-                       : path == RETOPK_PATH_FALLBACK ? CNT_FALLBACK : CNT_REFRESH], 1ull);
-        if (path == RETOPK_PATH_REUSE) {
-            atomicAdd(&cnt[CNT_SUM_M], (unsigned long long)N);
-            atomicMax(&cnt[CNT_MAX_M], (unsigned long long)N);
-        }
-        // the last head of the sequence to finish advances the ring and t_dec
-        __threadfence();
-        const int prev = atomicAdd(&w.seq[b * SEQ_WORDS + SEQ_DONE], 1);
-        if (prev == w.Hq - 1) {
-            __threadfence();
-            int *sq = w.seq + b * SEQ_WORDS;
-            const int head = *(volatile int *)&sq[SEQ_HEAD];
-            const int count = *(volatile int *)&sq[SEQ_COUNT];
-            sq[SEQ_HEAD] = (head + 1) % w.C;
-            sq[SEQ_COUNT] = min(count + 1, w.C);
-            sq[SEQ_TDEC] = *(volatile int *)&sq[SEQ_TDEC] + 1;
-            sq[SEQ_DONE] = 0;
-        }
-    }
+    if (a.mode == FIN_DECODE && tid == 0)
+        finish_head(w, b, path, N);
 }
 
 static size_t fin_smem_bytes(int K)

@@ -1,0 +1,214 @@
+// topk.cuh -- block-wide building blocks of the Top-K selection shared by the
+// reuse-path kernel and the exact-path finalize kernel (ReTopK paper, Eq. (1)
+// and Eq. (11): the K best keys by score, ties to the lower index).
+//
+// Candidates are visited through a callable get(j, idx, key) returning the
+// key index and the order-preserving score key of candidate j.
+#pragma once
+
+#include "common.cuh"
+
+namespace retopk {
+
+// Exclusive scan of one int per thread over an NT-thread block.  warp_tot
+// needs 33 ints of shared memory.  Three barriers; every thread must call it.
+template <int NT>
+__device__ __forceinline__ int block_excl_scan(int v, int *warp_tot, int &total)
+{
+    static_assert(NT % 32 == 0 && NT <= 1024, "block size");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o)
+            x += y;
+    }
+    if (lane == 31)
+        warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        const int w = lane < NT / 32 ? warp_tot[lane] : 0;
+        int s = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o)
+                s += y;
+        }
+        if (lane < NT / 32)
+            warp_tot[lane] = s - w;
+        if (lane == NT / 32 - 1)
+            warp_tot[32] = s;
+    }
+    __syncthreads();
+    const int r = warp_tot[warp] + x - v;
+    total = warp_tot[32];
+    __syncthreads();
+    return r;
+}
+
+struct SelectShared {
+    uint32_t hist[2][256];
+    int digit, above, cnt_d;
+    int warp_tot[33];
+};
+
+// Threshold of the `need` largest composite keys key64(key, idx) among N
+// candidates (radix select, 8-bit digits, most significant first; stops as soon
+// as every key sharing the current prefix is selected).  Returns thr with
+// |{j : key64_j >= thr}| == need; 0 when N <= need.  Identical in every thread.
+template <int NT, class Get>
+__device__ unsigned long long radix_select_threshold(int N, int need, Get get, SelectShared &sh)
+{
+    if (N <= need)
+        return 0ull;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < 512; i += NT)
+        (&sh.hist[0][0])[i] = 0u;
+    __syncthreads();
+    unsigned long long prefix = 0ull;
+    int rem = need;
+    int buf = 0;
+    for (int shift = 56; shift >= 0; shift -= 8, buf ^= 1) {
+        const unsigned long long hmask = (shift == 56) ? 0ull : (~0ull << (shift + 8));
+        uint32_t *hist = sh.hist[buf];
+        for (int j = tid; j < N; j += NT) {
+            int32_t idx;
+            uint32_t key;
+            get(j, idx, key);
+            const unsigned long long k64 = key64(key, idx);
+            if (((k64 ^ prefix) & hmask) == 0ull)
+                atomicAdd(&hist[(k64 >> shift) & 255ull], 1u);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            int c8[8];
+            int t8 = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                c8[i] = (int)hist[lane * 8 + i];
+                t8 += c8[i];
+            }
+            int sfx = t8;   // inclusive suffix over lanes >= lane
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_down_sync(0xffffffffu, sfx, o);
+                if (lane + o < 32)
+                    sfx += y;
+            }
+            int above = sfx - t8;
+            if (above < rem && rem <= sfx) {
+                for (int i = 7; i >= 0; --i) {
+                    if (above + c8[i] >= rem) {
+                        sh.digit = lane * 8 + i;
+                        sh.above = above;
+                        sh.cnt_d = c8[i];
+                        break;
+                    }
+                    above += c8[i];
+                }
+            }
+        } else if (warp == 1) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)   // the other buffer, for the next pass
+                sh.hist[buf ^ 1][lane * 8 + i] = 0u;
+        }
+        __syncthreads();
+        rem -= sh.above;
+        prefix |= (unsigned long long)sh.digit << shift;
+        if (sh.cnt_d == rem)
+            break;
+    }
+    return prefix;
+}
+
+// Stable compaction of the candidates with key64 >= thr, in candidate order,
+// into out_i / out_k (at most cap entries).  The outputs may alias the
+// candidate arrays read by `get` (positions written never exceed the position
+// read, and every read of a chunk precedes its writes).  Returns the count.
+template <int NT, class Get>
+__device__ int stable_compact(int N, unsigned long long thr, Get get, int cap, int32_t *out_i,
+                              uint32_t *out_k, int *warp_tot)
+{
+    int got = 0;
+    for (int base = 0; base < N; base += NT) {
+        const int j = base + threadIdx.x;
+        int32_t idx = 0;
+        uint32_t key = 0;
+        int flag = 0;
+        if (j < N) {
+            get(j, idx, key);
+            flag = key64(key, idx) >= thr;
+        }
+        int total;
+        const int pos = block_excl_scan<NT>(flag, warp_tot, total);
+        if (flag && got + pos < cap) {
+            out_i[got + pos] = idx;
+            out_k[got + pos] = key;
+        }
+        got += total;
+    }
+    return got < cap ? got : cap;
+}
+
+// Softmax-weighted partial sum over support rows [j0, j1) (stride `step` per
+// warp): lane l accumulates dims 4l..4l+3 with weights exp(score - m).
+// 16 rows in flight per lane.
+__device__ __forceinline__ void value_partial(const uint16_t *vb, const int32_t *sup_i, const uint32_t *sup_k,
+                                              int j0, int j1, int step, float m, float (&acc)[4], float &zsum)
+{
+    const int lane = threadIdx.x & 31;
+    for (int jb = j0; jb < j1; jb += step * 16) {
+        uint2 vv[16];
+        float p[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int j = jb + u * step;
+            if (j < j1) {
+                vv[u] = *reinterpret_cast<const uint2 *>(vb + (size_t)sup_i[j] * kD + lane * 4);
+                p[u] = expf(key2f(sup_k[j]) - m);
+            } else {
+                vv[u] = make_uint2(0u, 0u);
+                p[u] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            zsum += p[u];
+            acc[0] += p[u] * bf16lo(vv[u].x);
+            acc[1] += p[u] * bf16hi(vv[u].x);
+            acc[2] += p[u] * bf16lo(vv[u].y);
+            acc[3] += p[u] * bf16hi(vv[u].y);
+        }
+    }
+}
+
+// Query-support cache insertion and per-sequence bookkeeping after a decode
+// step of head bh (called by one thread):
+//   counters, and -- when this is the last head of sequence b to finish --
+//   the ring advance (next slot, live count) and t_dec += 1.
+__device__ __forceinline__ void finish_head(const Work &w, int b, int path, int M)
+{
+    unsigned long long *cnt = w.counters + (size_t)b * CNT_WORDS;
+    atomicAdd(&cnt[path == RETOPK_PATH_REUSE ? CNT_REUSE : path == RETOPK_PATH_FALLBACK ? CNT_FALLBACK : CNT_REFRESH],
+              1ull);
+    if (path == RETOPK_PATH_REUSE) {
+        atomicAdd(&cnt[CNT_SUM_M], (unsigned long long)M);
+        atomicMax(&cnt[CNT_MAX_M], (unsigned long long)M);
+    }
+    // the ring advance only has to be visible to the next step's kernels, which
+    // the kernel boundary orders; the counter just elects the last head
+    const int prev = atomicAdd(&w.seq[b * SEQ_WORDS + SEQ_DONE], 1);
+    if (prev == w.Hq - 1) {
+        int *sq = w.seq + b * SEQ_WORDS;
+        const int head = *(volatile int *)&sq[SEQ_HEAD];
+        const int count = *(volatile int *)&sq[SEQ_COUNT];
+        sq[SEQ_HEAD] = (head + 1) % w.C;
+        sq[SEQ_COUNT] = min(count + 1, w.C);
+        sq[SEQ_TDEC] = *(volatile int *)&sq[SEQ_TDEC] + 1;
+        sq[SEQ_DONE] = 0;
+    }
+}
+
+}  // namespace retopk
