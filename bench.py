@@ -181,132 +181,140 @@ def reference_arm(args, w, rank, world):
 
 
 # ------------------------------------------------------------------------------
+def replica_workload(w, rank):
+    """Rank r runs its own independent replica: the same shapes, other seeds."""
+    from top_sparse_attention_exact_gb300 import synth
+    return synth.scaled(w, seeds=tuple(s + 1000 * rank for s in w.seeds)) if rank else w
+
+
+def max_over_ranks(value, dist, device):
+    """Max of a per-rank timing total over all ranks (the job's time)."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def timed_steps(fn_prepare, fn_step, steps, flush, stream):
+    """Per-step CUDA-event times (ms) of fn_step(t) for t in steps, flushing the
+    L2 and keeping the GPU busy (so no host gap lands inside the events)
+    before each one."""
+    import torch
+    ev = []
+    for t in steps:
+        flush()
+        torch.cuda._sleep(GPU_BUSY_CYCLES)
+        fn_prepare(t)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn_step(t)
+        b.record(stream)
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    return np.array([a.elapsed_time(b) for a, b in ev])
+
+
+def profiled_steps(fn_prepare, fn_step, steps, flush):
+    """Per-kernel in-graph times (us per step) from the library's event nodes."""
+    import torch
+    from top_sparse_attention_exact_gb300 import retopk
+    acc = {}
+    for t in steps:
+        flush()
+        torch.cuda._sleep(GPU_BUSY_CYCLES)
+        fn_prepare(t)
+        fn_step(t)
+        torch.cuda.synchronize()
+        for k, (n, ms) in retopk.profile_read().items():
+            if n:
+                acc.setdefault(k, []).append(ms * 1000.0)
+    return {k: float(np.mean(v)) for k, v in acc.items()}
+
+
 def our_arm(args, w, rank, world, dist):
     import torch
     from top_sparse_attention_exact_gb300 import synth
     from top_sparse_attention_exact_gb300 import retopk
-    from top_sparse_attention_exact_gb300.runner import DecodeRun, ExactRun, to_dev
+    from top_sparse_attention_exact_gb300.runner import DecodeRun, ExactRun
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-    # each rank runs its own independent replica (different sequences)
-    wr = synth.scaled(w, seeds=tuple(s + 1000 * rank for s in w.seeds)) if rank else w
+    wr = replica_workload(w, rank)
     arrays = synth.generate(wr)
     Wm = max(3, args.warmup)
     Kt = args.steps
     if Wm + Kt > wr.steps:
         raise SystemExit(f"--warmup + --steps must be <= {wr.steps} decode steps of {wr.name}")
+    timed_t = range(Wm, Wm + Kt)
+    stream = torch.cuda.current_stream()
+    flush = L2Flush(dev)
 
+    # ---- ReTopK decode: headline (clean graph, one replay per step) ---------
     dr = DecodeRun(wr, arrays=arrays, device=dev)
     init_state = dr.ctx.retopk_export_state() if rank == 0 else None
     dr.capture()
-    flush = L2Flush(dev)
-    stream = torch.cuda.current_stream()
-
     for t in range(Wm):
         dr.replay(t)
     c0 = dr.ctx.retopk_get_counters()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Kt)]
-    step_paths = []
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         wall0 = time.perf_counter()
-        for i in range(Kt):
-            t = Wm + i
-            flush()
-            torch.cuda._sleep(GPU_BUSY_CYCLES)   # keeps the GPU busy while the host enqueues
-            dr.stage(t)
-            ev[i][0].record(stream)
-            dr.graph.replay()
-            ev[i][1].record(stream)
-            dr.t = t + 1
-        torch.cuda.synchronize()
+        step_ms = timed_steps(dr.stage, lambda t: dr.graph.replay(), timed_t, flush, stream)
         wall = time.perf_counter() - wall0
-    step_ms = np.array([a.elapsed_time(b) for a, b in ev])
     c1 = dr.ctx.retopk_get_counters()
-    if dist:
-        dist.barrier()
     total_ms = float(step_ms.sum())
     if dist:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+        dist.barrier()
+        total_ms = max_over_ranks(total_ms, dist, dev)
     us_step = total_ms / Kt * 1000.0
-
-    # per-step path mix (eager re-run of the same timed steps on a fresh context,
-    # with the same inputs, to classify each step; timing is not taken here)
     mix = {k2: c1[k2] - c0[k2] for k2 in ("reuse", "fallback", "refresh")}
     head_steps = max(1, sum(mix.values()))
 
-    # ---- Exact Top-K on the same inputs (graph replay, same flush) ----------
+    # ---- Exact Top-K on the same inputs (clean graph) --------------------------
     ex = ExactRun(dr)
-    sl_ex = dr.seqlens                                # the cache already holds every timed row
-    L_save = sl_ex.clone()
-    q_buf = torch.empty_like(dr.q_dec[0])
-    s = torch.cuda.Stream(device=dev)
-    s.wait_stream(stream)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(s):
-        with torch.cuda.graph(g, stream=s):
-            retopk.exact_topk_attention_step(q_buf, dr.k_cache, dr.v_cache, sl_ex, wr.K, ex.out, ex.idx, ex.ws, s)
-    stream.wait_stream(s)
-    torch.cuda.synchronize()
-    ex_ms = []
-    for i in range(Kt):
-        t = Wm + i
-        flush()
-        torch.cuda._sleep(GPU_BUSY_CYCLES)
-        sl_ex.fill_(wr.L0 + t + 1)
-        q_buf.copy_(dr.q_dec[t])
-        a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        g.replay()
-        b2.record(stream)
-        ex_ms.append((a, b2))
-    torch.cuda.synchronize()
-    ex_ms = np.array([a.elapsed_time(b2) for a, b2 in ex_ms])
+    ex.capture()
+    ex_ms = timed_steps(lambda t: None, ex.replay, timed_t, flush, stream)
     us_exact = float(ex_ms.mean() * 1000.0)
 
-    # ---- scan kernel roofline: eager exact steps with CUDA events around the
-    #      scan launch (library-side timing), same flush between steps -------
-    retopk.profile_enable(True)
+    # ---- per-kernel breakdown: profiled graphs on a second trajectory ----------
+    retopk.profile_reset()
+    dp = DecodeRun(wr, arrays=arrays, device=dev)
+    dp.capture(profiled=True)
+    for t in range(Wm):
+        dp.replay(t)
     retopk.profile_read()
-    n_prof = min(Kt, 64)
-    for i in range(n_prof):
-        t = Wm + i
-        flush()
-        torch.cuda._sleep(GPU_BUSY_CYCLES)
-        sl_ex.fill_(wr.L0 + t + 1)
-        retopk.exact_topk_attention_step(dr.q_dec[t], dr.k_cache, dr.v_cache, sl_ex, wr.K, ex.out, ex.idx, ex.ws)
-    torch.cuda.synchronize()
-    n_scan, scan_ms = retopk.profile_read()
-    retopk.profile_enable(False)
-    sl_ex.copy_(L_save)
-    mean_L = np.mean([wr.L0 + Wm + i + 1 for i in range(n_prof)])
-    scan_bytes = wr.B * wr.Hkv * mean_L * wr.d * 2          # every K row once per GQA group
-    scan_us = scan_ms / max(n_scan, 1) * 1000.0
+    kern_decode = profiled_steps(dp.stage, lambda t: dp.graph.replay(), timed_t, flush)
+    retopk.profile_reset()
+    exp = ExactRun(dp)
+    exp.capture(profiled=True)
+    kern_exact = profiled_steps(lambda t: None, exp.replay, timed_t, flush)
+    retopk.profile_reset()
+    del dp, exp
+    mean_L = float(np.mean([wr.L0 + t + 1 for t in timed_t]))
+    scan_bytes = wr.B * wr.Hkv * mean_L * wr.d * 2            # every K row once per GQA group
+    scan_us = kern_exact["scan"]
     peak, peak_kind = measured_peak()
     achieved = scan_bytes / (scan_us * 1e-6) / 1e9
     traffic = None
     try:
         with open(os.path.join(ROOT, "profiles", "scan_traffic.json")) as f:
             tr = json.load(f)
-        if tr.get("kernel_hash") == kernel_hash():
-            traffic = float(tr["bytes_per_launch_at_128k"]) * (mean_L / 131073.0)
+        if tr.get("kernel_sha1") == kernel_hash():
+            traffic = float(tr["dram_bytes_per_launch"]) * (mean_L / float(tr["L"]))
     except Exception:
         traffic = None
 
-    # ---- end to end through the public API with host buffers --------------
+    # ---- end to end through the public API with host buffers --------------------
     e2e = None
     if not args.no_e2e:
         de = DecodeRun(wr, arrays=arrays, device=dev)
-        qh = torch.from_numpy(np.ascontiguousarray(arrays[3]).view(np.int16)).pin_memory()   # [steps,B,Hq,d]
+        qh = torch.from_numpy(np.ascontiguousarray(arrays[3]).view(np.int16)).pin_memory()
         kn = torch.from_numpy(np.ascontiguousarray(arrays[0][:, :, wr.L0:].transpose(2, 0, 1, 3)).view(np.int16)).pin_memory()
         vn = torch.from_numpy(np.ascontiguousarray(arrays[1][:, :, wr.L0:].transpose(2, 0, 1, 3)).view(np.int16)).pin_memory()
-        out_h = torch.empty((Kt + Wm, wr.B, wr.Hq, wr.d), dtype=torch.int16).pin_memory()
+        out_h = torch.empty((wr.steps, wr.B, wr.Hq, wr.d), dtype=torch.int16).pin_memory()
         qd_, kd_, vd_ = (torch.empty_like(qh[0], device=dev), torch.empty_like(kn[0], device=dev),
                          torch.empty_like(vn[0], device=dev))
 
@@ -321,23 +329,23 @@ def our_arm(args, w, rank, world, dist):
         for t in range(Wm):
             e2e_step(t)
         torch.cuda.synchronize()
-        e_ev = []
-        for i in range(Kt):
-            t = Wm + i
+        e_ms = []
+        for t in timed_t:
             flush()
+            torch.cuda.synchronize()
             a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             e2e_step(t)
             b2.record(stream)
-            e_ev.append((a, b2))
-        torch.cuda.synchronize()
-        e_us = float(np.mean([a.elapsed_time(b2) for a, b2 in e_ev]) * 1000.0)
-        e2e = {"value": e_us, "unit": UNIT,
+            b2.synchronize()
+            e_ms.append(a.elapsed_time(b2))
+        e2e = {"value": float(np.mean(e_ms) * 1000.0), "unit": UNIT,
                "h2d_bytes_per_step": int(qh[0].numel() * 2 + kn[0].numel() * 2 + vn[0].numel() * 2),
-               "d2h_bytes_per_step": int(out_h[0].numel() * 2)}
+               "d2h_bytes_per_step": int(out_h[0].numel() * 2),
+               "how": "eager public API calls, pinned-host inputs copied in and the output copied out each step"}
         del de
 
-    # ---- CPU oracle baseline on a bounded sample (rank 0 only) -------------
+    # ---- CPU oracle baseline on a bounded sample (rank 0 only) --------------------
     cpu = None
     if rank == 0 and not args.no_cpu:
         import oracle
@@ -363,14 +371,16 @@ def our_arm(args, w, rank, world, dist):
                    "refresh_share": mix["refresh"] / head_steps,
                    "mean_candidates": (c1["sum_M"] - c0["sum_M"]) / max(1, mix["reuse"]),
                    "step_us_p50": float(np.median(step_ms) * 1000), "step_us_p90": float(np.percentile(step_ms, 90) * 1000),
+                   "kernel_us_per_step_retopk": kern_decode, "kernel_us_per_step_exact": kern_exact,
                    "wall_s_timed_loop": wall},
-        "roofline": {"kernel": "scan_kernel (full-history QK + first radix digit)", "bound": "hbm",
+        "roofline": {"kernel": "scan_kernel (full-history QK + first radix digit), exact step", "bound": "hbm",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind, "traffic": traffic, "scan_us": scan_us,
-                     "algorithmic_bytes": scan_bytes, "launches_timed": n_scan},
+                     "algorithmic_bytes": scan_bytes,
+                     "timing": "CUDA event-record nodes around the scan inside the replayed exact-step graph"},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 6 * Kt,
+        "gpu_launches": 5 * Kt,
         "clocks": clocks,
     }
     if rank == 0:

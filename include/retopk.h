@@ -167,6 +167,13 @@ int retopk_import_state(retopk_ctx *ctx, const void *host_buf, size_t bytes, voi
  * Synchronises `stream`. */
 int retopk_get_status(retopk_ctx *ctx, uint32_t *bits, int clear, void *stream);
 
+/* Failure-path self-test: launches one thread that waits on a barrier nothing
+ * arrives on, gives up after `wait_cycles` SM clock cycles (0..8e9), sets
+ * RETOPK_STATUS_TIMEOUT in the context's status word and returns -- the same
+ * bounded-wait path every pipeline wait of the scan kernel takes.  The
+ * context stays usable.  Asynchronous on `stream`. */
+int retopk_selftest_wait(retopk_ctx *ctx, int64_t wait_cycles, void *stream);
+
 const char *retopk_strerror(int code);
 
 /* The CUDA runtime's message for the last CUDA error that made a call of this
@@ -194,12 +201,27 @@ int exact_topk_attention_step(const retopk_bf16 *q, const retopk_bf16 *k_cache,
 
 /* ---- profiling ----------------------------------------------------------- */
 
-/* Optional per-kernel timing: when enabled, every launch records CUDA events
- * around the full-history scan kernel on its stream; retopk_profile_read
- * returns the number of scan launches and their summed duration in ms since
- * the last read (synchronises).  Off by default; not for use during capture. */
+/* Kernel classes reported by retopk_profile_read. */
+#define RETOPK_PROF_APPEND   0   /* K/V row append                                 */
+#define RETOPK_PROF_REUSE    1   /* recall, path switch and the whole reuse path   */
+#define RETOPK_PROF_SCAN     2   /* full-history QK scan + first radix digit       */
+#define RETOPK_PROF_FILTER   3   /* candidate filter of the exact path             */
+#define RETOPK_PROF_FINALIZE 4   /* exact-path Top-K, softmax-value, cache insert  */
+#define RETOPK_PROF_CLEAR    5   /* histogram clear of the stateless exact step    */
+#define RETOPK_PROF_KERNELS  6
+
+/* Optional per-kernel timing (off by default).  While enabled, every launch of
+ * retopk_append_kv, retopk_decode_step and exact_topk_attention_step is
+ * bracketed by two CUDA events on its stream.  Launches made while the stream
+ * is being captured get event-record nodes inside the graph; those events are
+ * kept, so each replay re-times them.  retopk_profile_read (synchronises on the
+ * events) returns, per kernel class, the number of timed launches and their
+ * summed duration in milliseconds: eager launches since the previous read, plus
+ * the latest replay of every captured launch.  retopk_profile_reset drops all
+ * events (call it before destroying graphs that hold them). */
 int retopk_profile_enable(int on);
-int retopk_profile_read(int64_t *scan_launches, double *scan_ms);
+int retopk_profile_read(int64_t launches[RETOPK_PROF_KERNELS], double ms[RETOPK_PROF_KERNELS]);
+int retopk_profile_reset(void);
 
 #ifdef __cplusplus
 }

@@ -246,3 +246,23 @@ def test_state_round_trip_and_status_bits():
     from top_sparse_attention_exact_gb300.retopk import RetopkError
     with pytest.raises(RetopkError):
         dr.ctx.retopk_import_state(bad)
+
+
+def test_bounded_wait_expires_and_context_survives():
+    """A pipeline wait that nobody satisfies gives up, flags the status word,
+    and leaves the context usable (no trap, no hang)."""
+    w = synth.scaled(synth.WORKLOADS["qwen7b_16k"], L0=2048, steps=2, name="selftest")
+    dr = DecodeRun(w)
+    dr.ctx.retopk_selftest_wait(100_000_000)      # ~50 ms of SM clock
+    torch.cuda.synchronize()
+    assert dr.ctx.retopk_get_status(clear=True) & 0x8
+    assert dr.ctx.retopk_get_status() == 0
+    pre = dr.ctx.retopk_export_state()
+    dr.step(0)
+    torch.cuda.synchronize()
+    post = dr.ctx.retopk_export_state()
+    diag = dr.ctx.retopk_get_diagnostics()
+    errs, _ = compare_decode_step(pre, post, diag, dr.qd_host[0], dr.k_host, dr.v_host,
+                                  dr.seqlens.cpu().numpy(), w, dr.out.cpu().numpy().view(np.uint16), "after")
+    assert not errs, errs[:5]
+    assert dr.ctx.retopk_get_status() == 0

@@ -190,30 +190,60 @@ int check_cfg(const retopk_config *c)
 
 
 // ---- optional scan timing -------------------------------------------------
+// Optional per-kernel timing.  With profiling on, every launch of a decode or
+// exact step is bracketed by two CUDA events on its stream.  Outside stream
+// capture the events are recorded eagerly and consumed by the next read; under
+// capture they become event-record nodes of the graph (cudaEventRecordExternal)
+// and are kept, so every replay re-times them and every read reports the last
+// replay.
+struct Mark {
+    int id;
+    cudaEvent_t a, b;
+    bool graph;
+};
 struct Prof {
     std::mutex mu;
     bool on = false;
-    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev;
-    long long done_launches = 0;
-    double done_ms = 0.0;
+    std::vector<Mark> marks;
 } g_prof;
+
+bool capturing(cudaStream_t st)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    return cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive;
+}
+
+void record(cudaEvent_t e, cudaStream_t st, bool graph)
+{
+    if (graph)
+        cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
+    else
+        cudaEventRecord(e, st);
+}
+
+// Runs `launch` (returning cudaError_t) between two profiling events.
+template <class F>
+cudaError_t timed(int id, cudaStream_t st, F launch)
+{
+    if (!g_prof.on)
+        return launch();
+    Mark m{id, nullptr, nullptr, capturing(st)};
+    if (cudaEventCreate(&m.a) != cudaSuccess || cudaEventCreate(&m.b) != cudaSuccess) {
+        if (m.a)
+            cudaEventDestroy(m.a);
+        return launch();
+    }
+    record(m.a, st, m.graph);
+    const cudaError_t e = launch();
+    record(m.b, st, m.graph);
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    g_prof.marks.push_back(m);
+    return e;
+}
 
 int run_scan(const Work &w, QSrc q, const uint16_t *k, const int32_t *sl, int off, cudaStream_t st)
 {
-    cudaEvent_t e0 = nullptr, e1 = nullptr;
-    if (g_prof.on) {
-        if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
-            if (e0)
-                cudaEventDestroy(e0);
-            e0 = e1 = nullptr;
-        }
-    }
-    const cudaError_t e = launch_scan(w, q, k, sl, off, st, e0, e1);
-    if (e0) {
-        std::lock_guard<std::mutex> lk(g_prof.mu);
-        g_prof.ev.emplace_back(e0, e1);
-    }
-    return cuda_rc(e);
+    return cuda_rc(timed(RETOPK_PROF_SCAN, st, [&] { return launch_scan(w, q, k, sl, off, st); }));
 }
 
 // The scan is persistent: one CTA per SM shares the tiles of every active group.
@@ -318,7 +348,9 @@ int retopk_append_kv(retopk_ctx *ctx, const retopk_bf16 *k_new, const retopk_bf1
         return RETOPK_ERR_INVALID;
     if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
         return RETOPK_ERR_ALIGN;
-    return cuda_rc(launch_append(ctx->w, k_new, v_new, k_cache, v_cache, d_seqlens, (cudaStream_t)stream));
+    cudaStream_t st = (cudaStream_t)stream;
+    return cuda_rc(timed(RETOPK_PROF_APPEND, st,
+                         [&] { return launch_append(ctx->w, k_new, v_new, k_cache, v_cache, d_seqlens, st); }));
 }
 
 int retopk_decode_step(retopk_ctx *ctx, const retopk_bf16 *q, const retopk_bf16 *k_cache,
@@ -333,13 +365,16 @@ int retopk_decode_step(retopk_ctx *ctx, const retopk_bf16 *q, const retopk_bf16 
     const Work &w = ctx->w;
     QSrc qs{q, (long long)w.Hq * kD, kD};
     int e;
-    if ((e = cuda_rc(launch_reuse(w, q, k_cache, v_cache, d_seqlens, out, st))))
+    if ((e = cuda_rc(timed(RETOPK_PROF_REUSE, st,
+                           [&] { return launch_reuse(w, q, k_cache, v_cache, d_seqlens, out, st); }))))
         return e;
     if ((e = run_scan(w, qs, k_cache, d_seqlens, 0, st)))
         return e;
-    if ((e = cuda_rc(launch_filter(w, d_seqlens, 0, st))))
+    if ((e = cuda_rc(timed(RETOPK_PROF_FILTER, st, [&] { return launch_filter(w, d_seqlens, 0, st); }))))
         return e;
-    return cuda_rc(launch_finalize(w, qs, v_cache, d_seqlens, 0, FIN_DECODE, 0, out, nullptr, st));
+    return cuda_rc(timed(RETOPK_PROF_FINALIZE, st, [&] {
+        return launch_finalize(w, qs, v_cache, d_seqlens, 0, FIN_DECODE, 0, out, nullptr, st);
+    }));
 }
 
 int retopk_get_diagnostics(retopk_ctx *ctx, int32_t *path, float *rho_max, int32_t *topR, int32_t *M,
@@ -499,6 +534,13 @@ int retopk_get_status(retopk_ctx *ctx, uint32_t *bits, int clear, void *stream)
     return cuda_rc(e);
 }
 
+int retopk_selftest_wait(retopk_ctx *ctx, int64_t wait_cycles, void *stream)
+{
+    if (!ctx || wait_cycles < 0 || wait_cycles > 8000000000LL)
+        return RETOPK_ERR_INVALID;
+    return cuda_rc(launch_selftest_wait(ctx->w.status, (long long)wait_cycles, (cudaStream_t)stream));
+}
+
 const char *retopk_cuda_error_string(void)
 {
     return g_last_cuda_error == cudaSuccess ? "no CUDA error recorded" : cudaGetErrorString(g_last_cuda_error);
@@ -551,13 +593,16 @@ int exact_topk_attention_step(const retopk_bf16 *q, const retopk_bf16 *k_cache, 
     w.support = nullptr;
     cudaStream_t st = (cudaStream_t)stream;
     QSrc qs{q, (long long)Hq * kD, kD};
-    if ((e = cuda_rc(cudaMemsetAsync(w.hist, 0, (size_t)B * Hq * kHistBins * 4, st))))
+    if ((e = cuda_rc(timed(RETOPK_PROF_CLEAR, st,
+                           [&] { return cudaMemsetAsync(w.hist, 0, (size_t)B * Hq * kHistBins * 4, st); }))))
         return e;
     if ((e = run_scan(w, qs, k_cache, d_seqlens, 0, st)))
         return e;
-    if ((e = cuda_rc(launch_filter(w, d_seqlens, 0, st))))
+    if ((e = cuda_rc(timed(RETOPK_PROF_FILTER, st, [&] { return launch_filter(w, d_seqlens, 0, st); }))))
         return e;
-    return cuda_rc(launch_finalize(w, qs, v_cache, d_seqlens, 0, FIN_EXACT, 0, out, idx_out, st));
+    return cuda_rc(timed(RETOPK_PROF_FINALIZE, st, [&] {
+        return launch_finalize(w, qs, v_cache, d_seqlens, 0, FIN_EXACT, 0, out, idx_out, st);
+    }));
 }
 
 int retopk_profile_enable(int on)
@@ -567,28 +612,48 @@ int retopk_profile_enable(int on)
     return RETOPK_OK;
 }
 
-int retopk_profile_read(int64_t *scan_launches, double *scan_ms)
+int retopk_profile_read(int64_t launches[RETOPK_PROF_KERNELS], double ms[RETOPK_PROF_KERNELS])
 {
-    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev;
-    {
-        std::lock_guard<std::mutex> lk(g_prof.mu);
-        ev.swap(g_prof.ev);
+    if (!launches || !ms)
+        return RETOPK_ERR_INVALID;
+    for (int i = 0; i < RETOPK_PROF_KERNELS; ++i) {
+        launches[i] = 0;
+        ms[i] = 0.0;
     }
-    double ms = 0.0;
+    std::lock_guard<std::mutex> lk(g_prof.mu);
     int rc = RETOPK_OK;
-    for (auto &p : ev) {
+    std::vector<Mark> keep;
+    for (auto &m : g_prof.marks) {
         float t = 0.f;
-        if (cudaEventSynchronize(p.second) != cudaSuccess || cudaEventElapsedTime(&t, p.first, p.second) != cudaSuccess)
-            rc = RETOPK_ERR_CUDA;
-        ms += t;
-        cudaEventDestroy(p.first);
-        cudaEventDestroy(p.second);
+        cudaError_t e = cudaEventSynchronize(m.b);
+        if (e == cudaSuccess)
+            e = cudaEventElapsedTime(&t, m.a, m.b);
+        if (e == cudaSuccess && m.id >= 0 && m.id < RETOPK_PROF_KERNELS) {
+            launches[m.id] += 1;
+            ms[m.id] += t;
+        } else if (e != cudaSuccess && !m.graph) {
+            rc = cuda_rc(e);
+        }
+        if (m.graph) {
+            keep.push_back(m);
+        } else {
+            cudaEventDestroy(m.a);
+            cudaEventDestroy(m.b);
+        }
     }
-    if (scan_launches)
-        *scan_launches = (int64_t)ev.size();
-    if (scan_ms)
-        *scan_ms = ms;
+    g_prof.marks.swap(keep);
     return rc;
+}
+
+int retopk_profile_reset(void)
+{
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    for (auto &m : g_prof.marks) {
+        cudaEventDestroy(m.a);
+        cudaEventDestroy(m.b);
+    }
+    g_prof.marks.clear();
+    return RETOPK_OK;
 }
 
 }  // extern "C"

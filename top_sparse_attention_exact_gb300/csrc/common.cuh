@@ -127,6 +127,7 @@ cudaError_t launch_reuse(const Work &w, const uint16_t *q, const uint16_t *k_cac
 cudaError_t launch_append(const Work &w, const uint16_t *k_new, const uint16_t *v_new,
                           uint16_t *k_cache, uint16_t *v_cache, int32_t *seqlens, cudaStream_t st);
 cudaError_t launch_init_done(const Work &w, cudaStream_t st);
+cudaError_t launch_selftest_wait(uint32_t *status, long long limit, cudaStream_t st);
 cudaError_t configure_kernels();   // one-time function attributes (smem opt-in)
 int scan_ctas_per_sm();
 

@@ -90,13 +90,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 }
 
 // Bounded wait; returns false (and flags the status word) on expiry.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status)
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status,
+                                          long long limit = kWaitCycles)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > limit) {
             atomicOr(status, RETOPK_STATUS_TIMEOUT);
             return false;
         }
@@ -351,6 +352,25 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             mbar_wait(&sh.full[s], (last / S) & 1, a.status);
         }
     }
+}
+
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing
+// arrives on, gives up after `limit` cycles, flags RETOPK_STATUS_TIMEOUT and
+// returns -- the path every pipeline wait of the scan takes on expiry.
+__global__ void selftest_wait_kernel(uint32_t *status, long long limit)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_wait(&bar, 0, status, limit);
+    }
+}
+
+cudaError_t launch_selftest_wait(uint32_t *status, long long limit, cudaStream_t st)
+{
+    selftest_wait_kernel<<<1, 32, 0, st>>>(status, limit);
+    return cudaGetLastError();
 }
 
 // ---- host side --------------------------------------------------------------

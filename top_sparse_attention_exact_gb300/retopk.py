@@ -26,7 +26,10 @@ EXPORTED = ("retopk_workspace_bytes", "retopk_create", "retopk_destroy", "retopk
             "retopk_get_counters", "retopk_state_bytes", "retopk_export_state",
             "retopk_import_state", "retopk_get_status", "retopk_strerror", "retopk_cuda_error_string",
             "exact_topk_workspace_bytes", "exact_topk_attention_step",
-            "retopk_profile_enable", "retopk_profile_read")
+            "retopk_profile_enable", "retopk_profile_read", "retopk_profile_reset",
+            "retopk_selftest_wait")
+
+PROF_KERNELS = ("append", "reuse", "scan", "filter", "finalize", "clear")
 
 
 class RetopkError(RuntimeError):
@@ -69,6 +72,8 @@ def _declare(lib):
     lib.exact_topk_attention_step.argtypes = [_P, _P, _P, _P] + [_I] * 6 + [_P, _P, _P, _S, _P]
     lib.retopk_profile_enable.argtypes = [_I]
     lib.retopk_profile_read.argtypes = [_P, _P]
+    lib.retopk_profile_reset.argtypes = []
+    lib.retopk_selftest_wait.argtypes = [_P, ctypes.c_int64, _P]
     for name in EXPORTED:
         getattr(lib, name).restype = getattr(lib, name).restype or ctypes.c_int
     return lib
@@ -153,11 +158,17 @@ def profile_enable(on: bool):
     _check(load().retopk_profile_enable(1 if on else 0), "retopk_profile_enable")
 
 
-def profile_read():
-    n = ctypes.c_int64()
-    ms = ctypes.c_double()
-    _check(load().retopk_profile_read(ctypes.byref(n), ctypes.byref(ms)), "retopk_profile_read")
-    return n.value, ms.value
+def profile_read() -> dict:
+    """Per kernel class: (timed launches, summed ms) -- see retopk_profile_read."""
+    n = np.zeros(len(PROF_KERNELS), np.int64)
+    ms = np.zeros(len(PROF_KERNELS), np.float64)
+    _check(load().retopk_profile_read(n.ctypes.data_as(ctypes.c_void_p), ms.ctypes.data_as(ctypes.c_void_p)),
+           "retopk_profile_read")
+    return {k: (int(n[i]), float(ms[i])) for i, k in enumerate(PROF_KERNELS)}
+
+
+def profile_reset():
+    _check(load().retopk_profile_reset(), "retopk_profile_reset")
 
 
 class ReTopK:
@@ -247,6 +258,9 @@ class ReTopK:
         _check(load().retopk_get_status(self.handle, ctypes.byref(v), 1 if clear else 0, _stream(stream)),
                "retopk_get_status")
         return int(v.value)
+
+    def retopk_selftest_wait(self, wait_cycles: int, stream=None):
+        _check(load().retopk_selftest_wait(self.handle, int(wait_cycles), _stream(stream)), "retopk_selftest_wait")
 
     def _unpack(self, buf: np.ndarray) -> dict:
         B, Hq, C, K, d = self.B, self.Hq, self.C, self.K, self.d

@@ -12,7 +12,7 @@ import numpy as np
 import torch
 
 from . import synth
-from .retopk import ReTopK, exact_topk_attention_step, exact_topk_workspace_bytes
+from .retopk import ReTopK, exact_topk_attention_step, exact_topk_workspace_bytes, profile_enable
 
 
 def to_dev(a: np.ndarray, device) -> torch.Tensor:
@@ -54,7 +54,9 @@ class DecodeRun:
         return self.out
 
     # ---- CUDA graph: one capture, replayed with per-step staging copies ----
-    def capture(self):
+    def capture(self, profiled: bool = False):
+        """Capture append + decode as one graph; `profiled` embeds the library's
+        per-kernel timing events in it (read them with retopk.profile_read)."""
         w = self.w
         self.q_buf = torch.empty((w.B, w.Hq, w.d), dtype=torch.int16, device=self.device)
         self.k_buf = torch.empty((w.B, w.Hkv, w.d), dtype=torch.int16, device=self.device)
@@ -63,10 +65,16 @@ class DecodeRun:
         s = torch.cuda.Stream(device=self.device)
         s.wait_stream(torch.cuda.current_stream())
         g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(s):
-            with torch.cuda.graph(g, stream=s):
-                self.ctx.retopk_append_kv(self.k_buf, self.v_buf, self.k_cache, self.v_cache, self.seqlens, s)
-                self.ctx.retopk_decode_step(self.q_buf, self.k_cache, self.v_cache, self.seqlens, self.out, s)
+        if profiled:
+            profile_enable(True)
+        try:
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s):
+                    self.ctx.retopk_append_kv(self.k_buf, self.v_buf, self.k_cache, self.v_cache, self.seqlens, s)
+                    self.ctx.retopk_decode_step(self.q_buf, self.k_cache, self.v_cache, self.seqlens, self.out, s)
+        finally:
+            if profiled:
+                profile_enable(False)
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
         self.graph = g
@@ -96,8 +104,37 @@ class ExactRun:
         nb = exact_topk_workspace_bytes(w.B, w.Hq, w.Hkv, w.d, dr.max_len, w.K)
         self.ws = torch.empty(nb + 256, dtype=torch.uint8, device=dr.device)
 
-    def step(self, q, stream=None):
+    def step(self, q, stream=None, seqlens=None):
         dr = self.dr
-        exact_topk_attention_step(q, dr.k_cache, dr.v_cache, dr.seqlens, dr.w.K, self.out, self.idx,
-                                  self.ws, stream)
+        sl = dr.seqlens if seqlens is None else seqlens
+        exact_topk_attention_step(q, dr.k_cache, dr.v_cache, sl, dr.w.K, self.out, self.idx, self.ws, stream)
+        return self.out
+
+    def capture(self, profiled: bool = False):
+        """One exact step on staging buffers (q_buf, seqlens_buf) as a graph."""
+        dr = self.dr
+        self.q_buf = torch.empty_like(dr.q_dec[0])
+        self.sl_buf = dr.seqlens.clone()
+        s = torch.cuda.Stream(device=dr.device)
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        if profiled:
+            profile_enable(True)
+        try:
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s):
+                    self.step(self.q_buf, s, self.sl_buf)
+        finally:
+            if profiled:
+                profile_enable(False)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.graph = g
+        return g
+
+    def replay(self, t: int):
+        """Exact step for decode step t's query over the first L0 + t + 1 keys."""
+        self.q_buf.copy_(self.dr.q_dec[t])
+        self.sl_buf.fill_(self.dr.w.L0 + t + 1)
+        self.graph.replay()
         return self.out
