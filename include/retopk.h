@@ -50,7 +50,8 @@ enum {
     RETOPK_ERR_WORKSPACE = -3,    /* workspace too small or misaligned              */
     RETOPK_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed           */
     RETOPK_ERR_ALIGN = -5,        /* a tensor pointer is not 16-byte aligned        */
-    RETOPK_ERR_STATE = -6         /* state buffer of the wrong size or version      */
+    RETOPK_ERR_STATE = -6,        /* state buffer of the wrong size or version      */
+    RETOPK_ERR_SCRATCH = -7       /* exceeds the static scratch of the _noalloc call */
 };
 
 /* Status bits (sticky, set by device code). */
@@ -198,6 +199,28 @@ int exact_topk_attention_step(const retopk_bf16 *q, const retopk_bf16 *k_cache,
                               int B, int Hq, int Hkv, int d, int max_len, int K,
                               retopk_bf16 *out, int32_t *idx_out,
                               void *d_workspace, size_t bytes, void *stream);
+
+/* Allocation-free variant of exact_topk_attention_step (the paper has no
+ * counterpart; it exists for callers that cannot allocate device memory at
+ * all -- code where allocation is forbidden or unavailable, e.g. an external
+ * memory manager owning the whole device, or a plain C host with no allocator
+ * to provide a workspace).  Same inputs, outputs and results as
+ * exact_topk_attention_step, but the scratch comes from one 16 MiB file-scope
+ * device array in the library instead of a caller workspace, so the call
+ * allocates nothing (no cudaMalloc / cudaFree, no allocating library call).
+ *   - Sizes whose workspace (exact_topk_workspace_bytes) exceeds 16 MiB are
+ *     rejected with RETOPK_ERR_SCRATCH before anything is launched (at
+ *     Hq = 28, Hkv = 4, K = 512 and B = 1 that allows max_len <= 48960).
+ *   - The array is shared by every call in the process and keeps the last
+ *     call's contents; each call clears what must start at zero.  Calls that
+ *     overlap on the GPU (other streams, other threads) race on it.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ * Every GPU that loads the library holds the 16 MiB until the process exits. */
+int exact_topk_attention_step_noalloc(const retopk_bf16 *q, const retopk_bf16 *k_cache,
+                                      const retopk_bf16 *v_cache, const int32_t *d_seqlens,
+                                      int B, int Hq, int Hkv, int d, int max_len, int K,
+                                      retopk_bf16 *out, int32_t *idx_out, void *stream);
 
 /* ---- profiling ----------------------------------------------------------- */
 

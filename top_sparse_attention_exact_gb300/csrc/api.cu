@@ -253,6 +253,37 @@ int n_scan_for(int B, int Hkv, int max_len)
     return (int)std::max(1LL, std::min<long long>(sm_count() * scan_ctas_per_sm(), tiles));
 }
 
+// Scratch of exact_topk_attention_step_noalloc: 16 MiB held by every GPU that
+// loads the library, for as long as the process lives.  Every call shares it,
+// so calls that overlap on the GPU race.
+constexpr size_t kNoallocScratchBytes = 16u << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+// Device address of the array on the current device, looked up once per
+// device (with that device current) on the first call made there.
+int noalloc_scratch(void **out)
+{
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static void *addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess)
+        return cuda_rc(ce);
+    if (dev < 0 || dev >= kMaxDevices)
+        return RETOPK_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        ce = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (ce != cudaSuccess)
+            return cuda_rc(ce);
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return RETOPK_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -556,6 +587,7 @@ const char *retopk_strerror(int code)
     case RETOPK_ERR_CUDA: return "CUDA runtime error";
     case RETOPK_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
     case RETOPK_ERR_STATE: return "state buffer of the wrong size or with invalid contents";
+    case RETOPK_ERR_SCRATCH: return "sizes need more scratch than the library's 16 MiB static array";
     default: return "unknown error";
     }
 }
@@ -603,6 +635,33 @@ int exact_topk_attention_step(const retopk_bf16 *q, const retopk_bf16 *k_cache, 
     return cuda_rc(timed(RETOPK_PROF_FINALIZE, st, [&] {
         return launch_finalize(w, qs, v_cache, d_seqlens, 0, FIN_EXACT, 0, out, idx_out, st);
     }));
+}
+
+// ---- allocation-free Exact Top-K step ---------------------------------------
+// For callers that cannot allocate device memory at all: code running where
+// allocation is forbidden or unavailable (inside a decode loop that must not
+// touch the allocator, under an external memory manager that owns every byte
+// of the device, or from a plain C host that has no allocator of its own to
+// hand out a workspace).  The scratch the exact path needs lives in one
+// file-scope device array instead of a caller-provided workspace.
+int exact_topk_attention_step_noalloc(const retopk_bf16 *q, const retopk_bf16 *k_cache,
+                                      const retopk_bf16 *v_cache, const int32_t *d_seqlens, int B, int Hq,
+                                      int Hkv, int d, int max_len, int K, retopk_bf16 *out, int32_t *idx_out,
+                                      void *stream)
+{
+    int e = check_dims(B, Hq, Hkv, d, max_len, K);
+    if (e)
+        return e;
+    retopk_config c{B, Hq, Hkv, d, max_len, K, 1, 0, 1, 0, 0.f};
+    if (plan(c, false, nullptr, nullptr) > kNoallocScratchBytes)
+        return RETOPK_ERR_SCRATCH;
+    void *scratch = nullptr;
+    if ((e = noalloc_scratch(&scratch)))
+        return e;
+    // the existing exact path, with its workspace carved from the static array
+    // (it clears the only buffer that must start at zero, the score histogram)
+    return exact_topk_attention_step(q, k_cache, v_cache, d_seqlens, B, Hq, Hkv, d, max_len, K, out, idx_out,
+                                     scratch, kNoallocScratchBytes, stream);
 }
 
 int retopk_profile_enable(int on)

@@ -27,7 +27,7 @@ EXPORTED = ("retopk_workspace_bytes", "retopk_create", "retopk_destroy", "retopk
             "retopk_import_state", "retopk_get_status", "retopk_strerror", "retopk_cuda_error_string",
             "exact_topk_workspace_bytes", "exact_topk_attention_step",
             "retopk_profile_enable", "retopk_profile_read", "retopk_profile_reset",
-            "retopk_selftest_wait")
+            "retopk_selftest_wait", "exact_topk_attention_step_noalloc")
 
 PROF_KERNELS = ("append", "reuse", "scan", "filter", "finalize", "clear")
 
@@ -74,6 +74,7 @@ def _declare(lib):
     lib.retopk_profile_read.argtypes = [_P, _P]
     lib.retopk_profile_reset.argtypes = []
     lib.retopk_selftest_wait.argtypes = [_P, ctypes.c_int64, _P]
+    lib.exact_topk_attention_step_noalloc.argtypes = [_P, _P, _P, _P] + [_I] * 6 + [_P, _P, _P]
     for name in EXPORTED:
         getattr(lib, name).restype = getattr(lib, name).restype or ctypes.c_int
     return lib
@@ -151,6 +152,17 @@ def exact_topk_attention_step(q, k_cache, v_cache, seqlens, K, out, idx_out=None
         max_len, int(K), _ptr(_bf16(out)), _ptr(idx_out) if idx_out is not None else None,
         ctypes.c_void_p(wp), avail, _stream(stream))
     _check(rc, "exact_topk_attention_step")
+    return out
+
+
+def exact_topk_attention_step_noalloc(q, k_cache, v_cache, seqlens, K, out, idx_out=None, stream=None):
+    """Exact Top-K attention with the library's static scratch (no workspace)."""
+    B, Hq, d = q.shape
+    Hkv, max_len = k_cache.shape[1], k_cache.shape[2]
+    rc = load().exact_topk_attention_step_noalloc(
+        _ptr(_bf16(q)), _ptr(_bf16(k_cache)), _ptr(_bf16(v_cache)), _ptr(_i32(seqlens)), B, Hq, Hkv, d,
+        max_len, int(K), _ptr(_bf16(out)), _ptr(idx_out) if idx_out is not None else None, _stream(stream))
+    _check(rc, "exact_topk_attention_step_noalloc")
     return out
 
 
