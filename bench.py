@@ -380,7 +380,7 @@ def our_arm(args, w, rank, world, dist):
                      "timing": "CUDA event-record nodes around the scan inside the replayed exact-step graph"},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 5 * Kt,
+        "gpu_launches": 4 * Kt,
         "clocks": clocks,
     }
     if rank == 0:

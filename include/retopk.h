@@ -228,10 +228,10 @@ int exact_topk_attention_step_noalloc(const retopk_bf16 *q, const retopk_bf16 *k
 #define RETOPK_PROF_APPEND   0   /* K/V row append                                 */
 #define RETOPK_PROF_REUSE    1   /* recall, path switch and the whole reuse path   */
 #define RETOPK_PROF_SCAN     2   /* full-history QK scan + first radix digit       */
-#define RETOPK_PROF_FILTER   3   /* candidate filter of the exact path             */
-#define RETOPK_PROF_FINALIZE 4   /* exact-path Top-K, softmax-value, cache insert  */
-#define RETOPK_PROF_CLEAR    5   /* histogram clear of the stateless exact step    */
-#define RETOPK_PROF_KERNELS  6
+#define RETOPK_PROF_SELECT   3   /* exact path: candidate filter, Top-K,
+                                    softmax-value, cache insert                    */
+#define RETOPK_PROF_CLEAR    4   /* histogram clear of the stateless exact step    */
+#define RETOPK_PROF_KERNELS  5
 
 /* Optional per-kernel timing (off by default).  While enabled, every launch of
  * retopk_append_kv, retopk_decode_step and exact_topk_attention_step is

@@ -92,6 +92,45 @@ def test_exact_many_score_ties():
         assert idx[0, h].tolist() == sup.tolist()        # exact ties are resolved identically
 
 
+def test_exact_ties_beyond_shared_staging():
+    # 20000 equal scores: every key is a candidate, more than one CTA stages in
+    # shared memory, so the selection runs over the global candidate segments
+    rng = np.random.default_rng(5)
+    row = synth.random_bf16(rng, (128,))
+    k = np.broadcast_to(row, (1, 1, 20000, 128)).copy()
+    v = synth.random_bf16(rng, (1, 1, 20000, 128))
+    q = synth.random_bf16(rng, (1, 2, 128))
+    idx, out = run_exact(q, k, v, [20000], 300)
+    for h in range(2):
+        assert idx[0, h].tolist() == list(range(300))
+        ok, mx, rel = out_close(out[0, h], synth.bf16_bits_to_f32(v[0, 0, :300]).astype(np.float64).mean(0))
+        assert ok, (mx, rel)
+
+
+def test_exact_one_segment_holds_most_candidates():
+    # 1500 tied top scores inside the first of 8 candidate segments (more than
+    # a segment keeps in shared memory), the other 14884 keys far below
+    rng = np.random.default_rng(6)
+    q = synth.random_bf16(rng, (1, 1, 128), 1.0)
+    qf = synth.bf16_bits_to_f32(q[0, 0]).astype(np.float64)
+    k = synth.random_bf16(rng, (1, 1, 16384, 128), 0.05)
+    top = synth.f32_to_bf16_bits((2.0 * qf / np.linalg.norm(qf)).astype(np.float32))
+    k[0, 0, :1500] = top
+    v = synth.random_bf16(rng, (1, 1, 16384, 128))
+    idx, out = run_exact(q, k, v, [16384], 512)
+    errs = compare_exact(q, k, v, [16384], 512, idx, out, "segment")
+    assert not errs, "\n".join(errs[:10])
+    assert idx[0, 0].tolist() == list(range(512))
+
+
+def test_exact_long_sequence_several_slices_per_segment():
+    # 150001 keys: each of the 8 segments spans more than one shared-memory slice
+    q, k, v = gauss(8, 1, 2, 1, 150001)
+    idx, out = run_exact(q, k, v, [150001], 512)
+    errs = compare_exact(q, k, v, [150001], 512, idx, out, "long")
+    assert not errs, "\n".join(errs[:10])
+
+
 @pytest.mark.parametrize("name", ["qwen7b_16k"])
 def test_exact_qwen_shape_all_heads(name):
     w = synth.scaled(synth.WORKLOADS[name], steps=1)

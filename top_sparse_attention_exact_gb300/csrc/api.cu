@@ -82,7 +82,7 @@ int ensure_configured()
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
-int n_filter_for(int max_len) { return std::min(kMaxSeg, std::max(1, (max_len + 8191) / 8192)); }
+int n_filter_for(int) { return kExactCluster; }
 
 int cand_stride_for(int max_len, int n_filter, int RKW)
 {
@@ -364,9 +364,7 @@ int retopk_init_cache(retopk_ctx *ctx, const retopk_bf16 *q_last, const retopk_b
             return e;
         if ((e = run_scan(w, qc, k_cache, d_prompt_len, off, st)))
             return e;
-        if ((e = cuda_rc(launch_filter(w, d_prompt_len, off, st))))
-            return e;
-        if ((e = cuda_rc(launch_finalize(w, qc, k_cache, d_prompt_len, off, FIN_INIT, c, nullptr, nullptr, st))))
+        if ((e = cuda_rc(launch_exact_select(w, qc, k_cache, d_prompt_len, off, FIN_INIT, c, nullptr, nullptr, st))))
             return e;
     }
     return cuda_rc(launch_init_done(w0, st));
@@ -401,10 +399,8 @@ int retopk_decode_step(retopk_ctx *ctx, const retopk_bf16 *q, const retopk_bf16 
         return e;
     if ((e = run_scan(w, qs, k_cache, d_seqlens, 0, st)))
         return e;
-    if ((e = cuda_rc(timed(RETOPK_PROF_FILTER, st, [&] { return launch_filter(w, d_seqlens, 0, st); }))))
-        return e;
-    return cuda_rc(timed(RETOPK_PROF_FINALIZE, st, [&] {
-        return launch_finalize(w, qs, v_cache, d_seqlens, 0, FIN_DECODE, 0, out, nullptr, st);
+    return cuda_rc(timed(RETOPK_PROF_SELECT, st, [&] {
+        return launch_exact_select(w, qs, v_cache, d_seqlens, 0, FIN_DECODE, 0, out, nullptr, st);
     }));
 }
 
@@ -630,10 +626,8 @@ int exact_topk_attention_step(const retopk_bf16 *q, const retopk_bf16 *k_cache, 
         return e;
     if ((e = run_scan(w, qs, k_cache, d_seqlens, 0, st)))
         return e;
-    if ((e = cuda_rc(timed(RETOPK_PROF_FILTER, st, [&] { return launch_filter(w, d_seqlens, 0, st); }))))
-        return e;
-    return cuda_rc(timed(RETOPK_PROF_FINALIZE, st, [&] {
-        return launch_finalize(w, qs, v_cache, d_seqlens, 0, FIN_EXACT, 0, out, idx_out, st);
+    return cuda_rc(timed(RETOPK_PROF_SELECT, st, [&] {
+        return launch_exact_select(w, qs, v_cache, d_seqlens, 0, FIN_EXACT, 0, out, idx_out, st);
     }));
 }
 

@@ -17,8 +17,7 @@ constexpr int kMaxGroup = 16;       // query heads per KV head
 constexpr int kMaxLen = 1 << 20;    // rows per sequence (candidate bitmap in smem)
 constexpr int kMaxK = 4096;
 constexpr int kMaxC = 256;
-constexpr int kStageCap = 12288;    // candidates staged in shared memory by finalize
-constexpr int kMaxSeg = 64;         // filter CTAs (segments) per head
+constexpr int kExactCluster = 8;    // CTAs (candidate segments) per exact-path head
 constexpr int kMaxSeqGroups = 512;  // B * Hkv handled by one scan launch
 constexpr int kMaxCand = 20480;     // R*K + W (the candidate list lives in smem)
 
@@ -32,7 +31,7 @@ struct Work {
     int B, Hq, Hkv, G, max_len, K, C, W, R, T_r;
     float tau;
     int cand_stride;   // per-head capacity of cand_idx / cand_key
-    int n_filter;      // filter CTAs (segments) per head
+    int n_filter;      // candidate segments per exact head (= kExactCluster)
     int n_scan;        // scan CTAs per (b, h_kv)
     int sc_stride;     // row stride of `scores` (max_len rounded up to 16)
     // query-support cache (decode contexts only)
@@ -99,6 +98,65 @@ __device__ __forceinline__ int warp_isum(int v)
     return v;
 }
 
+// ---- mbarrier / bulk-copy helpers (inline PTX) --------------------------------
+constexpr long long kWaitCycles = 4000000000LL;   // bounded waits: ~2 s at 2 GHz
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait; returns false (and flags the status word) on expiry.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status,
+                                          long long limit = kWaitCycles)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > limit) {
+            atomicOr(status, RETOPK_STATUS_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// 1-D bulk copy global -> shared (TMA), completing on `bar`.  dst, src 16-byte
+// aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 // Effective length of sequence b for a launch (len_off < 0 during cache
 // initialisation, where the causal prefix of a prompt position is scored).
 // Clamped to the cache capacity so that a bad length can never index past it.
@@ -118,10 +176,9 @@ struct QSrc {              // where the query of (b, h) lives
 // ev0 / ev1 (optional) are recorded immediately around the kernel launch.
 cudaError_t launch_scan(const Work &w, QSrc q, const uint16_t *k_cache, const int32_t *seqlens,
                         int len_off, cudaStream_t st, cudaEvent_t ev0 = nullptr, cudaEvent_t ev1 = nullptr);
-cudaError_t launch_filter(const Work &w, const int32_t *seqlens, int len_off, cudaStream_t st);
-cudaError_t launch_finalize(const Work &w, QSrc q, const uint16_t *v_cache, const int32_t *seqlens,
-                            int len_off, int mode, int init_slot, uint16_t *out, int32_t *idx_out,
-                            cudaStream_t st);
+cudaError_t launch_exact_select(const Work &w, QSrc q, const uint16_t *v_cache, const int32_t *seqlens,
+                                int len_off, int mode, int init_slot, uint16_t *out, int32_t *idx_out,
+                                cudaStream_t st);
 cudaError_t launch_reuse(const Work &w, const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                          const int32_t *seqlens, uint16_t *out, cudaStream_t st);
 cudaError_t launch_append(const Work &w, const uint16_t *k_new, const uint16_t *v_new,

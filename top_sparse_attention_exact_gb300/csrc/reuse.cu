@@ -23,7 +23,7 @@
 // after a second barrier rank 0 normalises, writes the output and inserts
 // (q_t, S_t) into the query-support cache (Eq. (5)).
 // Heads on the exact path only publish their path here (and clear their score
-// histogram for the scan); the scan / filter / finalize kernels serve them.
+// histogram for the scan); the scan and exact-select kernels serve them.
 #include <cooperative_groups.h>
 
 #include <algorithm>

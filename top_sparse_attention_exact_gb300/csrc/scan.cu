@@ -42,7 +42,6 @@ constexpr int kStageBytes = kTileRows * kD * 2;          // 32 KiB
 constexpr int kConsumerWarps = 8;
 constexpr int kScanThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxGroups = kMaxSeqGroups;                // B * Hkv
-constexpr long long kWaitCycles = 4000000000LL;          // ~2 s at 2 GHz
 
 struct ScanArgs {
     const uint16_t *q;
@@ -56,55 +55,6 @@ struct ScanArgs {
     float scale;
 };
 
-// ---- PTX helpers ----------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait; returns false (and flags the status word) on expiry.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status,
-                                          long long limit = kWaitCycles)
-{
-    if (mbar_try_wait(bar, parity))
-        return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > limit) {
-            atomicOr(status, RETOPK_STATUS_TIMEOUT);
-            return false;
-        }
-    }
-    return true;
-}
-
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
                                             uint64_t policy)
 {
@@ -114,6 +64,13 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)),
           "l"(policy)
         : "memory");
+}
+
+// fp32 store with an L2 evict-last policy: the scores are re-read right after
+// the scan while the K stream (evict-first) passes through L2.
+__device__ __forceinline__ void st_keep(float *p, float v, uint64_t policy)
+{
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(policy) : "memory");
 }
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -235,6 +192,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     } else {
         // ================= consumers =================
         const int g = lane >> 2, t = lane & 3;
+        uint64_t keep;
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
         int gi = -1;
         uint32_t mask = 0;
         int b = 0, hk = 0, L = 0;
@@ -325,7 +284,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                     const int r = (e < 2) ? r0 : r1;
                     if (n < G && r < L && ((mask >> n) & 1u)) {
                         const float sc = c[nt][e] * a.scale + 0.0f;
-                        sc_base[(size_t)n * a.sc_stride + r] = sc;
+                        st_keep(&sc_base[(size_t)n * a.sc_stride + r], sc, keep);
                         atomicAdd(&hist_s[n * kHistBins + (f2key(sc) >> (32 - kHistBits))], 1u);
                     }
                 }

@@ -1,5 +1,5 @@
 // topk.cuh -- block-wide building blocks of the Top-K selection shared by the
-// reuse-path kernel and the exact-path finalize kernel (ReTopK paper, Eq. (1)
+// reuse-path kernel and the exact-path select kernel (ReTopK paper, Eq. (1)
 // and Eq. (11): the K best keys by score, ties to the lower index).
 //
 // Candidates are visited through a callable get(j, idx, key) returning the
@@ -52,26 +52,25 @@ struct SelectShared {
     uint32_t hist[2][256];
     int digit, above, cnt_d;
     int warp_tot[33];
+    unsigned long long kand[32], kor[32];
 };
 
-// Threshold of the `need` largest composite keys key64(key, idx) among N
-// candidates (radix select, 8-bit digits, most significant first; stops as soon
-// as every key sharing the current prefix is selected).  Returns thr with
-// |{j : key64_j >= thr}| == need; 0 when N <= need.  Identical in every thread.
+// Radix refinement of a select threshold: the keys whose bits [top, 64) equal
+// those of `prefix` compete for `rem` (>= 1) slots (keys above the prefix are
+// already selected); 8-bit digits, most significant first, stopping as soon
+// as every key sharing the current prefix is selected.  On entry sh.hist[0]
+// is zero and a barrier has passed since.  Returns the threshold (identical
+// in every thread).
 template <int NT, class Get>
-__device__ unsigned long long radix_select_threshold(int N, int need, Get get, SelectShared &sh)
+__device__ unsigned long long radix_refine(int N, int rem, unsigned long long prefix, int top, Get get,
+                                          SelectShared &sh)
 {
-    if (N <= need)
-        return 0ull;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < 512; i += NT)
-        (&sh.hist[0][0])[i] = 0u;
-    __syncthreads();
-    unsigned long long prefix = 0ull;
-    int rem = need;
     int buf = 0;
-    for (int shift = 56; shift >= 0; shift -= 8, buf ^= 1) {
-        const unsigned long long hmask = (shift == 56) ? 0ull : (~0ull << (shift + 8));
+    for (int hi = top; hi > 0; hi -= 8, buf ^= 1) {
+        const int lo = hi > 8 ? hi - 8 : 0;          // digit = bits [lo, hi)
+        const unsigned long long hmask = (hi >= 64) ? 0ull : (~0ull << hi);
+        const unsigned dmask = (1u << (hi - lo)) - 1u;
         uint32_t *hist = sh.hist[buf];
         for (int j = tid; j < N; j += NT) {
             int32_t idx;
@@ -79,7 +78,7 @@ __device__ unsigned long long radix_select_threshold(int N, int need, Get get, S
             get(j, idx, key);
             const unsigned long long k64 = key64(key, idx);
             if (((k64 ^ prefix) & hmask) == 0ull)
-                atomicAdd(&hist[(k64 >> shift) & 255ull], 1u);
+                atomicAdd(&hist[(unsigned)(k64 >> lo) & dmask], 1u);
         }
         __syncthreads();
         if (warp == 0) {
@@ -116,36 +115,94 @@ __device__ unsigned long long radix_select_threshold(int N, int need, Get get, S
         }
         __syncthreads();
         rem -= sh.above;
-        prefix |= (unsigned long long)sh.digit << shift;
+        prefix |= (unsigned long long)sh.digit << lo;
         if (sh.cnt_d == rem)
             break;
     }
     return prefix;
 }
 
-// Stable compaction of the candidates with key64 >= thr, in candidate order,
-// into out_i / out_k (at most cap entries).  The outputs may alias the
-// candidate arrays read by `get` (positions written never exceed the position
-// read, and every read of a chunk precedes its writes).  Returns the count.
+// Threshold of the `need` largest composite keys key64(key, idx) among N
+// candidates: a radix select that starts at the highest bit where the
+// candidates differ (the bits above are common to all of them).  Returns thr
+// with |{j : key64_j >= thr}| == need; 0 when N <= need.  Identical in every
+// thread.
 template <int NT, class Get>
+__device__ unsigned long long radix_select_threshold(int N, int need, Get get, SelectShared &sh)
+{
+    if (N <= need)
+        return 0ull;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // common prefix: AND and OR of all keys
+    unsigned long long kand = ~0ull, kor = 0ull;
+    for (int j = tid; j < N; j += NT) {
+        int32_t idx;
+        uint32_t key;
+        get(j, idx, key);
+        const unsigned long long k64 = key64(key, idx);
+        kand &= k64;
+        kor |= k64;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        kand &= __shfl_xor_sync(0xffffffffu, kand, o);
+        kor |= __shfl_xor_sync(0xffffffffu, kor, o);
+    }
+    if (lane == 0) {
+        sh.kand[warp] = kand;
+        sh.kor[warp] = kor;
+    }
+    for (int i = tid; i < 512; i += NT)
+        (&sh.hist[0][0])[i] = 0u;
+    __syncthreads();
+    kand = ~0ull;
+    kor = 0ull;
+    for (int v = 0; v < NT / 32; ++v) {
+        kand &= sh.kand[v];
+        kor |= sh.kor[v];
+    }
+    const unsigned long long diff = kand ^ kor;      // nonzero: the indices differ
+    const int top = 64 - __clzll(diff);              // bits [top, 64) are common
+    const unsigned long long prefix = (top >= 64) ? 0ull : (kand & (~0ull << top));
+    return radix_refine<NT>(N, need, prefix, top, get, sh);
+}
+
+// Stable compaction of the candidates with key64 >= thr, in candidate order,
+// into out_i / out_k (at most cap entries).  Thread t handles E consecutive
+// candidates of each NT*E chunk, so one block scan covers the chunk.  The
+// outputs may alias the candidate arrays read by `get` (positions written never
+// exceed the position read, and every read of a chunk precedes its writes).
+// Returns the count.
+template <int NT, int E = 8, class Get>
 __device__ int stable_compact(int N, unsigned long long thr, Get get, int cap, int32_t *out_i,
                               uint32_t *out_k, int *warp_tot)
 {
     int got = 0;
-    for (int base = 0; base < N; base += NT) {
-        const int j = base + threadIdx.x;
-        int32_t idx = 0;
-        uint32_t key = 0;
-        int flag = 0;
-        if (j < N) {
-            get(j, idx, key);
-            flag = key64(key, idx) >= thr;
+    for (int base = 0; base < N; base += NT * E) {
+        const int j0 = base + threadIdx.x * E;
+        int32_t idx[E];
+        uint32_t key[E];
+        int c = 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            idx[e] = 0;
+            key[e] = 0u;
+            if (j0 + e < N) {
+                get(j0 + e, idx[e], key[e]);
+                c += key64(key[e], idx[e]) >= thr;
+            }
         }
         int total;
-        const int pos = block_excl_scan<NT>(flag, warp_tot, total);
-        if (flag && got + pos < cap) {
-            out_i[got + pos] = idx;
-            out_k[got + pos] = key;
+        int pos = got + block_excl_scan<NT>(c, warp_tot, total);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            if (j0 + e < N && key64(key[e], idx[e]) >= thr) {
+                if (pos < cap) {
+                    out_i[pos] = idx[e];
+                    out_k[pos] = key[e];
+                }
+                ++pos;
+            }
         }
         got += total;
     }
@@ -154,16 +211,17 @@ __device__ int stable_compact(int N, unsigned long long thr, Get get, int cap, i
 
 // Softmax-weighted partial sum over support rows [j0, j1) (stride `step` per
 // warp): lane l accumulates dims 4l..4l+3 with weights exp(score - m).
-// 16 rows in flight per lane.
+// U rows in flight per lane.
+template <int U = 16>
 __device__ __forceinline__ void value_partial(const uint16_t *vb, const int32_t *sup_i, const uint32_t *sup_k,
                                               int j0, int j1, int step, float m, float (&acc)[4], float &zsum)
 {
     const int lane = threadIdx.x & 31;
-    for (int jb = j0; jb < j1; jb += step * 16) {
-        uint2 vv[16];
-        float p[16];
+    for (int jb = j0; jb < j1; jb += step * U) {
+        uint2 vv[U];
+        float p[U];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int j = jb + u * step;
             if (j < j1) {
                 vv[u] = *reinterpret_cast<const uint2 *>(vb + (size_t)sup_i[j] * kD + lane * 4);
@@ -174,7 +232,7 @@ __device__ __forceinline__ void value_partial(const uint16_t *vb, const int32_t 
             }
         }
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
+        for (int u = 0; u < U; ++u) {
             zsum += p[u];
             acc[0] += p[u] * bf16lo(vv[u].x);
             acc[1] += p[u] * bf16hi(vv[u].x);
