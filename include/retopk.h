@@ -127,7 +127,10 @@ int retopk_append_kv(retopk_ctx *ctx, const retopk_bf16 *k_new, const retopk_bf1
  *   both:        Eq. (12) softmax-value aggregation over the support, then the
  *                cache insertion of (q, support) and t_dec += 1.
  * q: [B, Hq, d] bf16; out: [B, Hq, d] bf16.  No host round trip: the path
- * switch lives on the device, so the call can be captured in a CUDA graph. */
+ * switch lives on the device, so the call can be captured in a CUDA graph.
+ * Three kernels on `stream`: the path decision, the scan of the KV groups
+ * with an exact-path head, and one back-end launch serving every head on its
+ * path. */
 int retopk_decode_step(retopk_ctx *ctx, const retopk_bf16 *q, const retopk_bf16 *k_cache,
                        const retopk_bf16 *v_cache, const int32_t *d_seqlens,
                        retopk_bf16 *out, void *stream);
@@ -226,12 +229,13 @@ int exact_topk_attention_step_noalloc(const retopk_bf16 *q, const retopk_bf16 *k
 
 /* Kernel classes reported by retopk_profile_read. */
 #define RETOPK_PROF_APPEND   0   /* K/V row append                                 */
-#define RETOPK_PROF_REUSE    1   /* recall, path switch and the whole reuse path   */
+#define RETOPK_PROF_FINISH   1   /* decode back end: reuse path or exact select    */
 #define RETOPK_PROF_SCAN     2   /* full-history QK scan + first radix digit       */
 #define RETOPK_PROF_SELECT   3   /* exact path: candidate filter, Top-K,
                                     softmax-value, cache insert                    */
 #define RETOPK_PROF_CLEAR    4   /* histogram clear of the stateless exact step    */
-#define RETOPK_PROF_KERNELS  5
+#define RETOPK_PROF_DECIDE   5   /* recall, Top-R and path switch of a decode step */
+#define RETOPK_PROF_KERNELS  6
 
 /* Optional per-kernel timing (off by default).  While enabled, every launch of
  * retopk_append_kv, retopk_decode_step and exact_topk_attention_step is

@@ -13,7 +13,7 @@
 namespace retopk {
 cudaError_t configure_scan();
 cudaError_t configure_select();
-cudaError_t configure_reuse();
+cudaError_t configure_finish();
 }  // namespace retopk
 
 using namespace retopk;
@@ -75,7 +75,7 @@ int ensure_configured()
         if (err == cudaSuccess)
             err = configure_select();
         if (err == cudaSuccess)
-            err = configure_reuse();
+            err = configure_finish();
     });
     return cuda_rc(err);
 }
@@ -394,14 +394,14 @@ int retopk_decode_step(retopk_ctx *ctx, const retopk_bf16 *q, const retopk_bf16 
     const Work &w = ctx->w;
     QSrc qs{q, (long long)w.Hq * kD, kD};
     int e;
-    if ((e = cuda_rc(timed(RETOPK_PROF_REUSE, st,
-                           [&] { return launch_reuse(w, q, k_cache, v_cache, d_seqlens, out, st); }))))
+    // path decision (Eqs. (6), (7), (13)); the scan of the groups with an exact
+    // head; every head's back end in one launch
+    if ((e = cuda_rc(timed(RETOPK_PROF_DECIDE, st, [&] { return launch_decide(w, q, d_seqlens, st); }))))
         return e;
     if ((e = run_scan(w, qs, k_cache, d_seqlens, 0, st)))
         return e;
-    return cuda_rc(timed(RETOPK_PROF_SELECT, st, [&] {
-        return launch_exact_select(w, qs, v_cache, d_seqlens, 0, FIN_DECODE, 0, out, nullptr, st);
-    }));
+    return cuda_rc(timed(RETOPK_PROF_FINISH, st,
+                         [&] { return launch_finish(w, q, k_cache, v_cache, d_seqlens, out, st); }));
 }
 
 int retopk_get_diagnostics(retopk_ctx *ctx, int32_t *path, float *rho_max, int32_t *topR, int32_t *M,

@@ -148,6 +148,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
     return true;
 }
 
+// L2 prefetch of [src, src + bytes) by the bulk-copy engine (no completion to
+// wait for).  src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+                 : "memory");
+}
+
 // 1-D bulk copy global -> shared (TMA), completing on `bar`.  dst, src 16-byte
 // aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
@@ -175,17 +183,17 @@ struct QSrc {              // where the query of (b, h) lives
 
 // ev0 / ev1 (optional) are recorded immediately around the kernel launch.
 cudaError_t launch_scan(const Work &w, QSrc q, const uint16_t *k_cache, const int32_t *seqlens,
-                        int len_off, cudaStream_t st, cudaEvent_t ev0 = nullptr, cudaEvent_t ev1 = nullptr);
+                        int len_off, cudaStream_t st, int max_stages = 6);
 cudaError_t launch_exact_select(const Work &w, QSrc q, const uint16_t *v_cache, const int32_t *seqlens,
                                 int len_off, int mode, int init_slot, uint16_t *out, int32_t *idx_out,
                                 cudaStream_t st);
-cudaError_t launch_reuse(const Work &w, const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
-                         const int32_t *seqlens, uint16_t *out, cudaStream_t st);
+cudaError_t launch_decide(const Work &w, const uint16_t *q, const int32_t *seqlens, cudaStream_t st);
+cudaError_t launch_finish(const Work &w, const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                          const int32_t *seqlens, uint16_t *out, cudaStream_t st);
 cudaError_t launch_append(const Work &w, const uint16_t *k_new, const uint16_t *v_new,
                           uint16_t *k_cache, uint16_t *v_cache, int32_t *seqlens, cudaStream_t st);
 cudaError_t launch_init_done(const Work &w, cudaStream_t st);
 cudaError_t launch_selftest_wait(uint32_t *status, long long limit, cudaStream_t st);
-cudaError_t configure_kernels();   // one-time function attributes (smem opt-in)
 int scan_ctas_per_sm();
 
 enum { FIN_DECODE = 0, FIN_EXACT = 1, FIN_INIT = 2 };

@@ -1,0 +1,77 @@
+// finish.cu -- the back end of a decode step, after the path decision and the
+// scan: one cluster of kExactCluster CTAs per (sequence, query head) serves
+// the head on its path (ReTopK paper, Eq. (13)):
+//   reuse   -> reuse_body (reuse_body.cuh): Eqs. (8)-(12) over the candidates
+//              A_t, then the cache insertion;
+//   exact   -> exact_select_body (select_body.cuh): Eq. (1) over the scan's
+//              scores, Eq. (12), then the cache insertion.
+// Both kinds of head run side by side in one launch (the path is uniform over
+// a cluster); the two bodies overlay the same dynamic shared memory.
+#include "reuse_body.cuh"
+#include "select_body.cuh"
+
+namespace retopk {
+
+static_assert(kReuseThreads == kSelThreads && kReuseCluster == kExactCluster, "one launch shape for both paths");
+
+constexpr size_t kFinishMaxSmem = std::max(kReuseSharedBytes + ((size_t)(kMaxLen >> 5) + (size_t)kMaxCand) * 4,
+                                           kSelSharedBytes + kSelRegionBytes + (size_t)kLocCap * 8 +
+                                               (size_t)kMaxK * 8);
+static_assert(kFinishMaxSmem <= 227 * 1024, "largest configuration fits one CTA's shared memory");
+
+__global__ void __launch_bounds__(kSelThreads, 2) finish_kernel(SelArgs sa, ReuseArgs ra)
+{
+    extern __shared__ __align__(128) unsigned char fin_smem[];
+    if (sa.w.path[blockIdx.y] == RETOPK_PATH_REUSE)   // uniform over the cluster
+        reuse_body(ra, fin_smem);
+    else
+        exact_select_body(sa, fin_smem);
+}
+
+static size_t finish_smem_bytes(const Work &w)
+{
+    return std::max(sel_smem_bytes(w.K), reuse_smem_bytes(w.max_len, w.R * w.K + w.W));
+}
+
+cudaError_t launch_finish(const Work &w, const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                          const int32_t *seqlens, uint16_t *out, cudaStream_t st)
+{
+    SelArgs sa;
+    sa.w = w;
+    sa.q = q;
+    sa.q_b_stride = (long long)w.Hq * kD;
+    sa.q_h_stride = kD;
+    sa.v = v_cache;
+    sa.seqlens = seqlens;
+    sa.out = out;
+    sa.idx_out = nullptr;
+    sa.len_off = 0;
+    sa.mode = FIN_DECODE;
+    sa.init_slot = 0;
+    const ReuseArgs ra{w, q, k_cache, v_cache, seqlens, out, 1.0f / sqrtf((float)kD)};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kExactCluster, w.B * w.Hq, 1);
+    cfg.blockDim = dim3(kSelThreads, 1, 1);
+    cfg.dynamicSmemBytes = finish_smem_bytes(w);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kExactCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, finish_kernel, sa, ra);
+}
+
+cudaError_t configure_finish()
+{
+    cudaError_t e =
+        cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFinishMaxSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(finish_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+    return e;
+}
+
+}  // namespace retopk

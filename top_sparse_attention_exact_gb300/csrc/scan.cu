@@ -83,6 +83,28 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Adds the shared-memory histograms of the exact heads in `mask` (G heads of
+// kHistBins bins) into global memory: 16-byte shared loads, one atomic per
+// non-empty bin.  Called by the 256 consumer threads.
+__device__ __forceinline__ void flush_hist(const uint32_t *hist_s, uint32_t *hg, int G, uint32_t mask, int tid)
+{
+    constexpr int kVec = kHistBins / 4;
+    for (int i4 = tid; i4 < G * kVec; i4 += 256) {
+        if (!((mask >> (i4 / kVec)) & 1u))
+            continue;
+        const uint4 h = reinterpret_cast<const uint4 *>(hist_s)[i4];
+        uint32_t *d = hg + 4 * i4;
+        if (h.x)
+            atomicAdd(d + 0, h.x);
+        if (h.y)
+            atomicAdd(d + 1, h.y);
+        if (h.z)
+            atomicAdd(d + 2, h.z);
+        if (h.w)
+            atomicAdd(d + 3, h.w);
+    }
+}
+
 __device__ __forceinline__ void consumer_sync()
 {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
@@ -206,13 +228,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             if (ng != gi) {
                 consumer_sync();
                 if (gi >= 0) {   // flush the previous group's histogram
-                    uint32_t *hg = a.hist + (size_t)(b * a.Hq + hk * G) * kHistBins;
-                    for (int i = tid; i < G * kHistBins; i += kConsumerWarps * 32)
-                        if ((mask >> (i / kHistBins)) & 1u) {
-                            const uint32_t v = hist_s[i];
-                            if (v)
-                                atomicAdd(&hg[i], v);
-                        }
+                    flush_hist(hist_s, a.hist + (size_t)(b * a.Hq + hk * G) * kHistBins, G, mask, tid);
                     consumer_sync();
                 }
                 gi = ng;
@@ -220,9 +236,9 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 b = gi / a.Hkv;
                 hk = gi % a.Hkv;
                 L = seq_len(a.seqlens, b, a.len_off, a.max_len);
-                for (int i = tid; i < G * kHistBins; i += kConsumerWarps * 32)
-                    if ((mask >> (i / kHistBins)) & 1u)
-                        hist_s[i] = 0u;
+                for (int i4 = tid; i4 < G * (kHistBins / 4); i4 += kConsumerWarps * 32)
+                    if ((mask >> (i4 / (kHistBins / 4))) & 1u)
+                        reinterpret_cast<uint4 *>(hist_s)[i4] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const int n = nt * 8 + g;
@@ -291,15 +307,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             }
         }
         consumer_sync();
-        if (gi >= 0) {
-            uint32_t *hg = a.hist + (size_t)(b * a.Hq + hk * G) * kHistBins;
-            for (int i = tid; i < G * kHistBins; i += kConsumerWarps * 32)
-                if ((mask >> (i / kHistBins)) & 1u) {
-                    const uint32_t v = hist_s[i];
-                    if (v)
-                        atomicAdd(&hg[i], v);
-                }
-        }
+        if (gi >= 0)
+            flush_hist(hist_s, a.hist + (size_t)(b * a.Hq + hk * G) * kHistBins, G, mask, tid);
     }
     __syncthreads();
     // Drain: every issued copy has landed before shared memory is released
@@ -384,7 +393,7 @@ static cudaError_t make_kmap(CUtensorMap *map, const uint16_t *k, int B, int Hkv
 }
 
 cudaError_t launch_scan(const Work &w, QSrc q, const uint16_t *k_cache, const int32_t *seqlens,
-                        int len_off, cudaStream_t st, cudaEvent_t ev0, cudaEvent_t ev1)
+                        int len_off, cudaStream_t st, int max_stages)
 {
     if ((size_t)w.B * w.Hkv > (size_t)kMaxGroups)
         return cudaErrorInvalidValue;
@@ -408,19 +417,14 @@ cudaError_t launch_scan(const Work &w, QSrc q, const uint16_t *k_cache, const in
     a.max_len = w.max_len;
     a.sc_stride = w.sc_stride;
     a.len_off = len_off;
-    a.stages = stages_for(w.G);
+    a.stages = std::max(2, std::min(stages_for(w.G), max_stages));
     a.scale = 1.0f / sqrtf((float)kD);
-    const size_t smem = scan_smem_bytes(w.G);
-    if (ev0)
-        cudaEventRecord(ev0, st);
+    const size_t smem = 1024 + (size_t)a.stages * kStageBytes + hist_bytes(w.G);
     if (w.G <= 8)
         scan_kernel<1><<<w.n_scan, kScanThreads, smem, st>>>(map, a);
     else
         scan_kernel<2><<<w.n_scan, kScanThreads, smem, st>>>(map, a);
-    e = cudaGetLastError();
-    if (ev1)
-        cudaEventRecord(ev1, st);
-    return e;
+    return cudaGetLastError();
 }
 
 cudaError_t configure_scan()
@@ -428,10 +432,18 @@ cudaError_t configure_scan()
     size_t m1 = 0, m2 = 0;   // the largest request of each instantiation
     for (int G = 1; G <= kMaxGroup; ++G)
         (G <= 8 ? m1 : m2) = std::max(G <= 8 ? m1 : m2, scan_smem_bytes(G));
+    // the whole unified cache as shared memory: a decode-step scan CTA leaves
+    // room for a CTA of the concurrent reuse kernel only under that split
     cudaError_t e = cudaFuncSetAttribute(scan_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m1);
-    if (e != cudaSuccess)
-        return e;
-    return cudaFuncSetAttribute(scan_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m2);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(scan_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m2);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(scan_kernel<1>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(scan_kernel<2>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+    return e;
 }
 
 }  // namespace retopk

@@ -29,7 +29,7 @@ EXPORTED = ("retopk_workspace_bytes", "retopk_create", "retopk_destroy", "retopk
             "retopk_profile_enable", "retopk_profile_read", "retopk_profile_reset",
             "retopk_selftest_wait", "exact_topk_attention_step_noalloc")
 
-PROF_KERNELS = ("append", "reuse", "scan", "select", "clear")
+PROF_KERNELS = ("append", "finish", "scan", "select", "clear", "decide")
 
 
 class RetopkError(RuntimeError):
