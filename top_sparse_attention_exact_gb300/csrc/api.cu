@@ -113,12 +113,13 @@ size_t plan(const retopk_config &c, bool stateful, Work *w, char *base)
     x.sc_stride = (c.max_len + 15) & ~15;
     const size_t BH = (size_t)c.batch * c.n_q_heads;
     Layout L;
-    size_t o_fq = 0, o_fs = 0, o_fl = 0, o_seq = 0, o_cnt = 0, o_path = 0, o_rho = 0, o_topr = 0;
+    size_t o_fq = 0, o_fs = 0, o_fl = 0, o_seq = 0, o_snap = 0, o_cnt = 0, o_path = 0, o_rho = 0, o_topr = 0;
     if (stateful) {
         o_fq = L.add(BH * c.C * kD * 2);
         o_fs = L.add(BH * c.C * c.K * 4);
         o_fl = L.add(BH * c.C * 4);
         o_seq = L.add((size_t)c.batch * SEQ_WORDS * 4);
+        o_snap = L.add((size_t)c.batch * SEQ_WORDS * 4);
         o_cnt = L.add((size_t)c.batch * CNT_WORDS * 8);
         o_path = L.add(BH * 4);
         o_rho = L.add(BH * 4);
@@ -140,6 +141,7 @@ size_t plan(const retopk_config &c, bool stateful, Work *w, char *base)
             x.fifo_sup = (int32_t *)(base + o_fs);
             x.fifo_len = (int32_t *)(base + o_fl);
             x.seq = (int32_t *)(base + o_seq);
+            x.snap = (int32_t *)(base + o_snap);
             x.counters = (unsigned long long *)(base + o_cnt);
             x.path = (int32_t *)(base + o_path);
             x.rho_max = (float *)(base + o_rho);
@@ -508,7 +510,6 @@ static int state_copy(retopk_ctx *ctx, void *host, size_t bytes, cudaStream_t st
     } else if (e == cudaSuccess) {
         for (int b = 0; b < w.B; ++b) {
             memcpy(&seq[(size_t)b * SEQ_WORDS], p + b * 12, 12);
-            seq[(size_t)b * SEQ_WORDS + SEQ_DONE] = 0;
         }
         e = cudaMemcpyAsync(w.seq, seq.data(), seq.size() * 4, cudaMemcpyHostToDevice, st);
         if (e == cudaSuccess)

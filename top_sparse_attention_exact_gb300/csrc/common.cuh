@@ -22,7 +22,9 @@ constexpr int kMaxSeqGroups = 512;  // B * Hkv handled by one scan launch
 constexpr int kMaxCand = 20480;     // R*K + W (the candidate list lives in smem)
 
 // Per-sequence control words.
-enum { SEQ_HEAD = 0, SEQ_COUNT = 1, SEQ_TDEC = 2, SEQ_DONE = 3, SEQ_WORDS = 4 };
+// (next slot, live entries, decode steps done, unused); `snap` holds the same
+// three words as the path decision saw them, for the rest of the step.
+enum { SEQ_HEAD = 0, SEQ_COUNT = 1, SEQ_TDEC = 2, SEQ_WORDS = 4 };
 // Counters per sequence.
 enum { CNT_REUSE = 0, CNT_FALLBACK = 1, CNT_REFRESH = 2, CNT_SUM_M = 3, CNT_MAX_M = 4, CNT_WORDS = 5 };
 
@@ -39,6 +41,7 @@ struct Work {
     int32_t *fifo_sup;
     int32_t *fifo_len;
     int32_t *seq;
+    int32_t *snap;       // [B*SEQ_WORDS] this step's view of `seq`
     unsigned long long *counters;
     // per-step scratch
     int32_t *path;       // [B*Hq] (NULL: every head takes the exact path)
@@ -146,6 +149,42 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
         }
     }
     return true;
+}
+
+// Programmatic dependent launch.  A kernel launched with launch_pdl may start
+// while its predecessor on the stream is still running; pdl_wait() returns once
+// the predecessor grid has completed and its memory operations are visible
+// (at once for a plain launch).  pdl_trigger() lets this grid's successor
+// launch before this grid ends.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch with the programmatic-serialization attribute (and a cluster of
+// cluster_x CTAs along x when cluster_x > 1).
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       unsigned cluster_x, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
 }
 
 // L2 prefetch of [src, src + bytes) by the bulk-copy engine (no completion to

@@ -22,7 +22,23 @@ static_assert(kFinishMaxSmem <= 227 * 1024, "largest configuration fits one CTA'
 __global__ void __launch_bounds__(kSelThreads, 2) finish_kernel(SelArgs sa, ReuseArgs ra)
 {
     extern __shared__ __align__(128) unsigned char fin_smem[];
-    if (sa.w.path[blockIdx.y] == RETOPK_PATH_REUSE)   // uniform over the cluster
+    // Launched programmatically after the scan, so it may start while the scan
+    // runs.  A reuse head needs nothing from the scan: what it reads was
+    // written by the decision and the append, which completed before the scan
+    // passed its own wait (the scan lets this grid launch only after that).
+    // An exact head waits for the scan inside exact_select_body.
+    const Work &w = sa.w;
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y % w.Hq == 0) {
+        // the ring advance of Eq. (5) (slot, live count, t_dec): nothing later
+        // in this step reads `seq`, every head takes its slot from `snap`
+        const int b = blockIdx.y / w.Hq;
+        const int *sn = w.snap + b * SEQ_WORDS;
+        int *sq = w.seq + b * SEQ_WORDS;
+        sq[SEQ_HEAD] = (sn[SEQ_HEAD] + 1) % w.C;
+        sq[SEQ_COUNT] = min(sn[SEQ_COUNT] + 1, w.C);
+        sq[SEQ_TDEC] = sn[SEQ_TDEC] + 1;
+    }
+    if (w.path[blockIdx.y] == RETOPK_PATH_REUSE)   // uniform over the cluster
         reuse_body(ra, fin_smem);
     else
         exact_select_body(sa, fin_smem);
@@ -49,19 +65,8 @@ cudaError_t launch_finish(const Work &w, const uint16_t *q, const uint16_t *k_ca
     sa.mode = FIN_DECODE;
     sa.init_slot = 0;
     const ReuseArgs ra{w, q, k_cache, v_cache, seqlens, out, 1.0f / sqrtf((float)kD)};
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kExactCluster, w.B * w.Hq, 1);
-    cfg.blockDim = dim3(kSelThreads, 1, 1);
-    cfg.dynamicSmemBytes = finish_smem_bytes(w);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kExactCluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, finish_kernel, sa, ra);
+    return launch_pdl(finish_kernel, dim3(kExactCluster, w.B * w.Hq), dim3(kSelThreads), finish_smem_bytes(w), st, kExactCluster,
+                      sa, ra);
 }
 
 cudaError_t configure_finish()

@@ -28,13 +28,21 @@ struct DecideShared {
 __global__ void __launch_bounds__(kDecideThreads) decide_kernel(ReuseArgs a)
 {
     __shared__ DecideShared sh;
+    pdl_wait();      // the appended row and length, the previous step's cache update
+    pdl_trigger();   // the scan may set up while the decision runs
     const Work &w = a.w;
     const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = bh / w.Hq;
     const int L = seq_len(a.seqlens, b, 0, w.max_len);
     const int *sq = w.seq + b * SEQ_WORDS;
-    const int head = sq[SEQ_HEAD], count = sq[SEQ_COUNT];
-    const int t_dec = sq[SEQ_TDEC] + 1;
+    const int head = sq[SEQ_HEAD], count = sq[SEQ_COUNT], done = sq[SEQ_TDEC];
+    const int t_dec = done + 1;
+    if (tid == 0 && bh % w.Hq == 0) {   // the step's view of the ring, for the finish kernel
+        int *sn = w.snap + b * SEQ_WORDS;
+        sn[SEQ_HEAD] = head;
+        sn[SEQ_COUNT] = count;
+        sn[SEQ_TDEC] = done;
+    }
     if (tid < kD)
         sh.qf[tid] = __uint_as_float(((uint32_t)a.q[(size_t)bh * kD + tid]) << 16);
     const uint2 qraw = *reinterpret_cast<const uint2 *>(a.q + (size_t)bh * kD + lane * 4);
@@ -110,8 +118,7 @@ __global__ void __launch_bounds__(kDecideThreads) decide_kernel(ReuseArgs a)
 cudaError_t launch_decide(const Work &w, const uint16_t *q, const int32_t *seqlens, cudaStream_t st)
 {
     ReuseArgs a{w, q, nullptr, nullptr, seqlens, nullptr, 1.0f / sqrtf((float)kD)};
-    decide_kernel<<<w.B * w.Hq, kDecideThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(decide_kernel, dim3(w.B * w.Hq), dim3(kDecideThreads), 0, st, 1, a);
 }
 
 

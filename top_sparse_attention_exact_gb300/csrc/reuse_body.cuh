@@ -92,11 +92,14 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
 
     // ---- the decision's outputs: retrieved entries and their supports --------
     const int L = seq_len(a.seqlens, b, 0, w.max_len);
-    const int *sq = w.seq + b * SEQ_WORDS;
+    const int *sq = w.snap + b * SEQ_WORDS;   // the ring as the decision saw it
     const int head = sq[SEQ_HEAD], count = sq[SEQ_COUNT];
     const int nr = min(w.R, count);
+    const size_t e_slot = (size_t)bh * w.C + head;   // this step's cache entry (Eq. (5))
     if (tid < kD)
         sh.qf[tid] = __uint_as_float(((uint32_t)a.q[(size_t)bh * kD + tid]) << 16);
+    if (rank == 0 && tid < kD / 8)   // q_t into its slot, off the critical path (only the decision reads fifo_q)
+        reinterpret_cast<uint4 *>(w.fifo_q + e_slot * kD)[tid] = reinterpret_cast<const uint4 *>(a.q + (size_t)bh * kD)[tid];
     {   // slots, lengths and prefix of the nr (<= C <= kReuseThreads) retrieved supports
         int len = 0, off = 0;
         if (tid < nr) {
@@ -300,6 +303,21 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
     }
     __syncthreads();
     const float m = key2f(sh.kmax);
+    {   // S_t (identical in every rank), written 1/kReuseCluster per rank; every
+        // rank of the cluster is past its reads of the retrieved supports
+        const int kper = (w.K + kReuseCluster - 1) / kReuseCluster;
+        const int j0 = rank * kper, j1 = min(w.K, j0 + kper);
+        for (int jj = j0 + tid; jj < j1; jj += kReuseThreads) {
+            const int32_t v = jj < n ? sup_i[jj] : -1;
+            w.fifo_sup[e_slot * w.K + jj] = v;
+            w.support[(size_t)bh * w.K + jj] = v;
+        }
+        if (rank == 0 && tid == 0) {
+            w.fifo_len[e_slot] = n;
+            w.sup_len[bh] = n;
+            count_head(w, b, RETOPK_PATH_REUSE, M);
+        }
+    }
 
     // ---- Eq. (12): this rank's share of the value rows -----------------------
     const int vper = (n + kReuseCluster - 1) / kReuseCluster;
@@ -330,7 +348,7 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
     if (rank != 0)
         return;
 
-    // ---- rank 0: output, cache insertion, bookkeeping -------------------------
+    // ---- rank 0: the output ----------------------------------------------------
     if (tid < kD) {
         float o = 0.f, Z = 0.f;
 #pragma unroll
@@ -342,20 +360,7 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
         a.out[(size_t)bh * kD + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
         w.out_f32[(size_t)bh * kD + tid] = o;
     }
-    const int slot = head;
-    const size_t e = (size_t)bh * w.C + slot;
-    if (tid < kD / 8)
-        reinterpret_cast<uint4 *>(w.fifo_q + e * kD)[tid] = reinterpret_cast<const uint4 *>(a.q + (size_t)bh * kD)[tid];
-    for (int jj = tid; jj < w.K; jj += kReuseThreads) {
-        const int32_t v = jj < n ? sup_i[jj] : -1;
-        w.fifo_sup[e * w.K + jj] = v;
-        w.support[(size_t)bh * w.K + jj] = v;
-    }
-    if (tid == 0) {
-        w.fifo_len[e] = n;
-        w.sup_len[bh] = n;
-        finish_head(w, b, RETOPK_PATH_REUSE, M);
-    }
+
 }
 
 }  // namespace retopk

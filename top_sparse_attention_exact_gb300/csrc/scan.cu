@@ -138,6 +138,17 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         (reinterpret_cast<uintptr_t>(scan_smem) + 1023) & ~uintptr_t(1023));
     uint32_t *hist_s = reinterpret_cast<uint32_t *>(ring + (size_t)S * kStageBytes);   // [G][kHistBins]
 
+    // ---- set-up that needs nothing from the previous kernel
+    if (tid == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
+        for (int s2 = 0; s2 < S; ++s2) {
+            mbar_init(&sh.full[s2], 1);
+            mbar_init(&sh.empty[s2], kConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    pdl_wait();      // the path decision
+    pdl_trigger();
     // ---- active groups and their tile ranges (every CTA computes the same
     //      list): groups with no exact head get zero tiles
     const int NG = a.B * a.Hkv;
@@ -155,14 +166,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         sh.grp_mask[i] = mask;
         sh.grp_first[i + 1] = (mask && L > 0) ? (L + kTileRows - 1) / kTileRows : 0;
     }
-    if (tid == 0) {
+    if (tid == 0)
         sh.grp_first[0] = 0;
-        for (int s2 = 0; s2 < S; ++s2) {
-            mbar_init(&sh.full[s2], 1);
-            mbar_init(&sh.empty[s2], kConsumerWarps);
-        }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
     __syncthreads();
     // inclusive prefix over the per-group tile counts (one warp, NG <= 512)
     if (warp == 0) {
@@ -421,10 +426,8 @@ cudaError_t launch_scan(const Work &w, QSrc q, const uint16_t *k_cache, const in
     a.scale = 1.0f / sqrtf((float)kD);
     const size_t smem = 1024 + (size_t)a.stages * kStageBytes + hist_bytes(w.G);
     if (w.G <= 8)
-        scan_kernel<1><<<w.n_scan, kScanThreads, smem, st>>>(map, a);
-    else
-        scan_kernel<2><<<w.n_scan, kScanThreads, smem, st>>>(map, a);
-    return cudaGetLastError();
+        return launch_pdl(scan_kernel<1>, dim3(w.n_scan), dim3(kScanThreads), smem, st, 1, map, a);
+    return launch_pdl(scan_kernel<2>, dim3(w.n_scan), dim3(kScanThreads), smem, st, 1, map, a);
 }
 
 cudaError_t configure_scan()

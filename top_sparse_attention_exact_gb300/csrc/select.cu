@@ -30,19 +30,8 @@ cudaError_t launch_exact_select(const Work &w, QSrc q, const uint16_t *v_cache, 
     a.len_off = len_off;
     a.mode = mode;
     a.init_slot = init_slot;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kExactCluster, w.B * w.Hq, 1);
-    cfg.blockDim = dim3(kSelThreads, 1, 1);
-    cfg.dynamicSmemBytes = sel_smem_bytes(w.K);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kExactCluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, exact_select_kernel, a);
+    return launch_pdl(exact_select_kernel, dim3(kExactCluster, w.B * w.Hq), dim3(kSelThreads), sel_smem_bytes(w.K), st, kExactCluster,
+                      a);
 }
 
 cudaError_t configure_select()

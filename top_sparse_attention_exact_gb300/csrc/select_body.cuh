@@ -80,7 +80,6 @@ struct SelShared {
     alignas(16) uint32_t h2all[kExactCluster][kSubBins];   // every rank's h2 (pushed by the ranks)
     SelectShared sel;
     uint32_t kmax;
-    int slot;
     float zw[kSelWarps];
     alignas(16) float part_o[kExactCluster][kD];   // rank 0 receives every rank's partial
     float part_z[kExactCluster];
@@ -156,6 +155,14 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     const int path = (a.mode == FIN_DECODE) ? w.path[bh] : RETOPK_PATH_FALLBACK;
     if (path == RETOPK_PATH_REUSE)
         return;                                    // a reuse head (uniform over the cluster)
+    pdl_wait();                                    // the scan's scores and histogram
+    const bool insert = a.mode == FIN_DECODE || a.mode == FIN_INIT;   // into the query-support cache
+    const size_t e_slot = insert ? (size_t)bh * w.C + (a.mode == FIN_INIT ? a.init_slot : w.snap[b * SEQ_WORDS + SEQ_HEAD])
+                                 : 0;
+    if (insert && rank == 0 && tid < kD / 8) {     // q_t into its slot (Eq. (5)), off the critical path
+        const uint16_t *qrow = a.q + b * a.q_b_stride + (long long)h * a.q_h_stride;
+        reinterpret_cast<uint4 *>(w.fifo_q + e_slot * kD)[tid] = reinterpret_cast<const uint4 *>(qrow)[tid];
+    }
     const int L = seq_len(a.seqlens, b, a.len_off, w.max_len);
     const int need = min(w.K, L);
     const int seg = (((L + kExactCluster - 1) / kExactCluster) + 15) & ~15;
@@ -457,6 +464,27 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     }
     __syncthreads();
     const float m = key2f(sh.kmax);
+    {   // the support (identical in every rank), written 1/kExactCluster per rank
+        const int kper = (w.K + kExactCluster - 1) / kExactCluster;
+        const int j0 = rank * kper, j1 = min(w.K, j0 + kper);
+        for (int jj = j0 + tid; jj < j1; jj += kSelThreads) {
+            const int32_t v = jj < n ? sup_i[jj] : -1;
+            if (a.idx_out)
+                a.idx_out[(size_t)bh * w.K + jj] = v;
+            if (w.support)
+                w.support[(size_t)bh * w.K + jj] = v;
+            if (insert)
+                w.fifo_sup[e_slot * w.K + jj] = v;
+        }
+        if (rank == 0 && tid == 0) {
+            if (w.support)
+                w.sup_len[bh] = n;
+            if (insert)
+                w.fifo_len[e_slot] = n;
+            if (a.mode == FIN_DECODE)
+                count_head(w, b, path, N);
+        }
+    }
 
     // ---- 3. this rank's share of the value rows (Eq. (12)) -------------------
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -485,14 +513,12 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
             z += sh.zw[ww];
         cluster.map_shared_rank(&sh.part_z[0], 0)[rank] = z;
     }
-    if (tid == 0 && (a.mode == FIN_DECODE || a.mode == FIN_INIT))
-        sh.slot = (a.mode == FIN_INIT) ? a.init_slot : w.seq[b * SEQ_WORDS + SEQ_HEAD];
     cluster.sync();   // partials at rank 0; no rank reads a peer's shared memory after this
-    if (rank != 0)
+    if (rank != 0 || a.mode == FIN_INIT)
         return;
 
-    // ---- rank 0: output, support, cache insertion -----------------------------
-    if (a.mode != FIN_INIT && tid < kD) {
+    // ---- rank 0: the output ----------------------------------------------------
+    if (tid < kD) {
         float o = 0.f, Z = 0.f;
 #pragma unroll
         for (int r = 0; r < kExactCluster; ++r) {
@@ -504,27 +530,6 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
         if (w.out_f32)
             w.out_f32[(size_t)bh * kD + tid] = o;
     }
-    if (a.idx_out)
-        for (int jj = tid; jj < w.K; jj += kSelThreads)
-            a.idx_out[(size_t)bh * w.K + jj] = jj < n ? sup_i[jj] : -1;
-    if (w.support) {
-        for (int jj = tid; jj < w.K; jj += kSelThreads)
-            w.support[(size_t)bh * w.K + jj] = jj < n ? sup_i[jj] : -1;
-        if (tid == 0)
-            w.sup_len[bh] = n;
-    }
-    if (a.mode == FIN_DECODE || a.mode == FIN_INIT) {
-        const size_t e = (size_t)bh * w.C + sh.slot;
-        const uint16_t *qrow = a.q + b * a.q_b_stride + (long long)h * a.q_h_stride;
-        if (tid < kD / 8)
-            reinterpret_cast<uint4 *>(w.fifo_q + e * kD)[tid] = reinterpret_cast<const uint4 *>(qrow)[tid];
-        for (int jj = tid; jj < w.K; jj += kSelThreads)
-            w.fifo_sup[e * w.K + jj] = jj < n ? sup_i[jj] : -1;
-        if (tid == 0)
-            w.fifo_len[e] = n;
-    }
-    if (a.mode == FIN_DECODE && tid == 0)
-        finish_head(w, b, path, N);
 }
 
 

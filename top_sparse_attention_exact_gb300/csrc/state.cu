@@ -10,6 +10,8 @@ __global__ void append_kernel(const uint16_t *k_new, const uint16_t *v_new, uint
                               uint16_t *v_cache, int32_t *seqlens, uint32_t *status, int Hkv,
                               int max_len)
 {
+    pdl_wait();      // the previous step is done with the caches and the lengths
+    pdl_trigger();
     const int b = blockIdx.x;
     const int L = seqlens[b];
     if (L >= max_len) {
@@ -35,8 +37,8 @@ __global__ void append_kernel(const uint16_t *k_new, const uint16_t *v_new, uint
 cudaError_t launch_append(const Work &w, const uint16_t *k_new, const uint16_t *v_new,
                           uint16_t *k_cache, uint16_t *v_cache, int32_t *seqlens, cudaStream_t st)
 {
-    append_kernel<<<w.B, 128, 0, st>>>(k_new, v_new, k_cache, v_cache, seqlens, w.status, w.Hkv, w.max_len);
-    return cudaGetLastError();
+    return launch_pdl(append_kernel, dim3(w.B), dim3(128), 0, st, 1, k_new, v_new, k_cache, v_cache, seqlens,
+                      w.status, w.Hkv, w.max_len);
 }
 
 // After cache initialisation: C entries in slots 0..C-1, next slot 0, t_dec 0.
@@ -47,7 +49,6 @@ __global__ void init_done_kernel(int32_t *seq, unsigned long long *counters, int
         seq[b * SEQ_WORDS + SEQ_HEAD] = 0;
         seq[b * SEQ_WORDS + SEQ_COUNT] = C;
         seq[b * SEQ_WORDS + SEQ_TDEC] = 0;
-        seq[b * SEQ_WORDS + SEQ_DONE] = 0;
         for (int i = 0; i < CNT_WORDS; ++i)
             counters[(size_t)b * CNT_WORDS + i] = 0ull;
     }

@@ -242,11 +242,9 @@ __device__ __forceinline__ void value_partial(const uint16_t *vb, const int32_t 
     }
 }
 
-// Query-support cache insertion and per-sequence bookkeeping after a decode
-// step of head bh (called by one thread):
-//   counters, and -- when this is the last head of sequence b to finish --
-//   the ring advance (next slot, live count) and t_dec += 1.
-__device__ __forceinline__ void finish_head(const Work &w, int b, int path, int M)
+// Per-sequence counters after a decode step of one head (one thread; no
+// result is waited for): the head's path, and on the reuse path |A_t|.
+__device__ __forceinline__ void count_head(const Work &w, int b, int path, int M)
 {
     unsigned long long *cnt = w.counters + (size_t)b * CNT_WORDS;
     atomicAdd(&cnt[path == RETOPK_PATH_REUSE ? CNT_REUSE : path == RETOPK_PATH_FALLBACK ? CNT_FALLBACK : CNT_REFRESH],
@@ -254,18 +252,6 @@ __device__ __forceinline__ void finish_head(const Work &w, int b, int path, int 
     if (path == RETOPK_PATH_REUSE) {
         atomicAdd(&cnt[CNT_SUM_M], (unsigned long long)M);
         atomicMax(&cnt[CNT_MAX_M], (unsigned long long)M);
-    }
-    // the ring advance only has to be visible to the next step's kernels, which
-    // the kernel boundary orders; the counter just elects the last head
-    const int prev = atomicAdd(&w.seq[b * SEQ_WORDS + SEQ_DONE], 1);
-    if (prev == w.Hq - 1) {
-        int *sq = w.seq + b * SEQ_WORDS;
-        const int head = *(volatile int *)&sq[SEQ_HEAD];
-        const int count = *(volatile int *)&sq[SEQ_COUNT];
-        sq[SEQ_HEAD] = (head + 1) % w.C;
-        sq[SEQ_COUNT] = min(count + 1, w.C);
-        sq[SEQ_TDEC] = *(volatile int *)&sq[SEQ_TDEC] + 1;
-        sq[SEQ_DONE] = 0;
     }
 }
 
