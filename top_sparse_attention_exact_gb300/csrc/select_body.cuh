@@ -54,7 +54,16 @@ static_assert(kSubBins == 256, "second-level digit is 8 bits");
 // partials share one region (they are live in phases 1, 2 and 3)
 constexpr size_t kSelRegionBytes = (size_t)kSliceCap * 4 > (size_t)kSelStageCap * 8 ? (size_t)kSliceCap * 4
                                                                                    : (size_t)kSelStageCap * 8;
-static_assert(kSelRegionBytes >= (size_t)kSelWarps * kD * 4, "value partials fit the region");
+// Region layout after the filter: staging arrays st_idx [0, 32 KiB) and
+// st_key [32 KiB, 64 KiB); with at most kVPreCap final candidates the V rows
+// of a rank's share of them are copied to [kVPreOff, 32 KiB) while the Top-K
+// is selected; the per-warp value partials sit at kRedOff.
+constexpr size_t kVPreOff = 4096;
+constexpr int kVPreRows = (int)((32768 - kVPreOff) / (kD * 2));   // per rank
+constexpr int kVPreCap = kVPreRows * kExactCluster;
+constexpr size_t kRedOff = 40960;
+static_assert(kVPreOff >= (size_t)kVPreCap * 4 && 32768 + (size_t)kVPreCap * 4 <= kRedOff, "staging below the V rows");
+static_assert(kRedOff + (size_t)kSelWarps * kD * 4 <= kSelRegionBytes, "value partials fit the region");
 static_assert(kHistBins == 4 * kSelThreads, "one uint4 of histogram per thread");
 
 struct SelArgs {
@@ -69,7 +78,7 @@ struct SelArgs {
 };
 
 struct SelShared {
-    uint64_t bar;                                  // bulk-copy completion
+    uint64_t bar;                                  // bulk-copy completion (score slices)
     int T1, T2, above2;
     int wcnt[kSelWarps];                           // final candidates per rank (phase 2)
     uint8_t gmask[kMaxBlk * kBlkGroups];           // filter: bit e of group g = score 4g + e passes
@@ -174,7 +183,8 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     float *slice = reinterpret_cast<float *>(xs);                          // [kSliceCap], phase 1
     int32_t *st_idx = reinterpret_cast<int32_t *>(xs);                     // [kSelStageCap], phase 2
     uint32_t *st_key = reinterpret_cast<uint32_t *>(st_idx + kSelStageCap);
-    float(*red)[kD] = reinterpret_cast<float(*)[kD]>(xs);                  // [kSelWarps][kD], phase 3
+    uint16_t *vrows = reinterpret_cast<uint16_t *>(xs + kVPreOff);         // [kVPreRows][kD], phases 2-3
+    float(*red)[kD] = reinterpret_cast<float(*)[kD]>(xs + kRedOff);        // [kSelWarps][kD], phase 3
     int32_t *loc_i = reinterpret_cast<int32_t *>(xs + kSelRegionBytes);    // [kLocCap]
     uint32_t *loc_k = reinterpret_cast<uint32_t *>(loc_i + kLocCap);
     const int Kp = (w.K + 3) & ~3;
@@ -186,6 +196,7 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     if (tid == 0) {
         mbar_init(&sh.bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        sh.kmax = 0u;
         sh.T1 = 0;
         sh.T2 = 0;
         sh.above2 = -1;   // stays -1 unless digit T2 is found
@@ -384,6 +395,7 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
         const uint32_t *pk = local ? cluster.map_shared_rank(loc_k, r) : gk + (size_t)r * seg;
         const unsigned lt = (1u << lane) - 1u;
         int dst = sh.off[r];
+        uint32_t km = 0u;   // the largest key: the support's maximum (Eq. (12)'s shift)
         for (int j0 = 0; j0 < cr; j0 += 4 * 32) {
             int32_t ii[4];
             uint32_t kk[4];
@@ -400,10 +412,14 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
                 if (take) {
                     st_idx[dst + __popc(bal & lt)] = ii[u];
                     st_key[dst + __popc(bal & lt)] = kk[u];
+                    km = max(km, kk[u]);
                 }
                 dst += __popc(bal);
             }
         }
+        km = __reduce_max_sync(0xffffffffu, km);
+        if (lane == 0)
+            atomicMax(&sh.kmax, km);
     }
     if (staged)
         for (int i = tid; i < 512; i += kSelThreads)
@@ -419,12 +435,30 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
         idx = st_idx[j];
         k = st_key[j];
     };
+    // With few final candidates, rank r's 1/kExactCluster of them (in staging
+    // order) get their V rows copied to shared memory now (16-byte asynchronous
+    // copies from every thread) while the Top-K is selected; Eq. (12) then
+    // sums over that share with weight 0 for the candidates outside the
+    // support.
+    const bool vpre = staged && N2 <= kVPreCap && a.mode != FIN_INIT;
+    const int cper = (N2 + kExactCluster - 1) / kExactCluster;
+    const int vc0 = min(N2, rank * cper), vc1 = min(N2, vc0 + cper);
+    const uint16_t *vb = a.v + ((size_t)(b * w.Hkv + hk) * w.max_len) * kD;
+    if (vpre) {
+        constexpr int kChunks = kD * 2 / 16;   // 16-byte pieces of a row
+        for (int c = tid; c < (vc1 - vc0) * kChunks; c += kSelThreads) {
+            const int j = vc0 + c / kChunks, part = c % kChunks;
+            cp_async16(vrows + (size_t)(j - vc0) * kD + part * 8, vb + (size_t)st_idx[j] * kD + part * 8);
+        }
+        cp_async_commit();
+    }
     int n;
+    unsigned long long thr = 0ull;
     if (staged) {
         // every key above prefix (T1, T2) is in; the need - above2 others come
         // from the keys with that prefix (a histogram that disagreed with the
         // scores -- no T2 found -- falls back to the full select)
-        const unsigned long long thr =
+        thr =
             N2 <= need       ? 0ull
             : sh.above2 >= 0 ? radix_refine<kSelThreads>(N2, need - sh.above2,
                                                          (unsigned long long)p19 << (32 + kSub), 32 + kSub,
@@ -448,13 +482,9 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
             idx = gi[o];
             k = gk[o];
         };
-        const unsigned long long thr = radix_select_threshold<kSelThreads>(N, need, get_global, sh.sel);
+        thr = radix_select_threshold<kSelThreads>(N, need, get_global, sh.sel);
         n = stable_compact<kSelThreads, 4>(N, thr, get_global, w.K, sup_i, sup_k, sh.sel.warp_tot);
-    }
-    if (tid == 0)
-        sh.kmax = 0u;
-    __syncthreads();   // also: the staging arrays are dead from here (the region holds `red`)
-    {
+        __syncthreads();
         uint32_t km = 0u;
         for (int j = tid; j < n; j += kSelThreads)
             km = max(km, sup_k[j]);
@@ -489,10 +519,24 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     // ---- 3. this rank's share of the value rows (Eq. (12)) -------------------
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float zsum = 0.f;
-    if (a.mode != FIN_INIT) {   // cache initialisation needs the support only
+    if (vpre) {
+        cp_async_wait_all();
+        __syncthreads();
+        for (int j = vc0 + warp; j < vc1; j += kSelWarps) {   // warp-uniform
+            const uint32_t k = st_key[j];
+            if (key64(k, st_idx[j]) < thr)
+                continue;                                     // not in the support
+            const float p = expf(key2f(k) - m);
+            const uint2 vv = *reinterpret_cast<const uint2 *>(vrows + (size_t)(j - vc0) * kD + lane * 4);
+            zsum += p;
+            acc[0] += p * bf16lo(vv.x);
+            acc[1] += p * bf16hi(vv.x);
+            acc[2] += p * bf16lo(vv.y);
+            acc[3] += p * bf16hi(vv.y);
+        }
+    } else if (a.mode != FIN_INIT) {   // cache initialisation needs the support only
         const int vper = (n + kExactCluster - 1) / kExactCluster;
         const int vs = min(n, rank * vper), ve = min(n, vs + vper);
-        const uint16_t *vb = a.v + ((size_t)(b * w.Hkv + hk) * w.max_len) * kD;
         value_partial<8>(vb, sup_i, sup_k, vs + warp, ve, kSelWarps, m, acc, zsum);
     }
     *reinterpret_cast<float4 *>(&red[warp][lane * 4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
