@@ -2,9 +2,10 @@
 """Decode-attention benchmark: ReTopK and Exact Top-K on one synthetic
 Qwen2.5-7B-shaped layer (28 query heads over 4 KV heads, d = 128, bf16).
 
-One step = one decode step of one layer: append the token's K/V row, then
-retopk_decode_step (recall, path switch, candidate union, rerank, Top-K,
-softmax-value aggregation, cache update), replayed as one CUDA graph.
+One step = one decode step of one layer: retopk_decode_step_kv (append the
+token's K/V row, recall, path switch, full-history scan of the groups with an
+exact-path head, candidate union, rerank, Top-K, softmax-value aggregation,
+cache update: three kernels), replayed as one CUDA graph.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -322,8 +323,7 @@ def our_arm(args, w, rank, world, dist):
             qd_.copy_(qh[t], non_blocking=True)
             kd_.copy_(kn[t], non_blocking=True)
             vd_.copy_(vn[t], non_blocking=True)
-            de.ctx.retopk_append_kv(kd_, vd_, de.k_cache, de.v_cache, de.seqlens)
-            de.ctx.retopk_decode_step(qd_, de.k_cache, de.v_cache, de.seqlens, de.out)
+            de.ctx.retopk_decode_step_kv(kd_, vd_, qd_, de.k_cache, de.v_cache, de.seqlens, de.out)
             out_h[t].copy_(de.out, non_blocking=True)
 
         for t in range(Wm):
@@ -380,7 +380,7 @@ def our_arm(args, w, rank, world, dist):
                      "timing": "CUDA event-record nodes around the scan inside the replayed exact-step graph"},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 4 * Kt,
+        "gpu_launches": 3 * Kt,
         "clocks": clocks,
     }
     if rank == 0:

@@ -135,6 +135,16 @@ int retopk_decode_step(retopk_ctx *ctx, const retopk_bf16 *q, const retopk_bf16 
                        const retopk_bf16 *v_cache, const int32_t *d_seqlens,
                        retopk_bf16 *out, void *stream);
 
+/* retopk_append_kv followed by retopk_decode_step, in one fewer launch: the
+ * path-decision kernel also writes the new K/V rows and advances the length
+ * (same results, same KV_FULL behaviour; the ReTopK paper has no separate
+ * notion of this fusion -- it is the decode step with the token's K/V append
+ * of Eq. (4)'s L_t folded in).  k_new / v_new: [B, Hkv, d] bf16.
+ * Graph-capturable. */
+int retopk_decode_step_kv(retopk_ctx *ctx, const retopk_bf16 *k_new, const retopk_bf16 *v_new,
+                          const retopk_bf16 *q, retopk_bf16 *k_cache, retopk_bf16 *v_cache,
+                          int32_t *d_seqlens, retopk_bf16 *out, void *stream);
+
 /* Per-step diagnostics of the last decode step, copied to HOST buffers
  * (synchronises `stream`).  Any pointer may be NULL.
  *   path     [B*Hq] int32   RETOPK_PATH_*

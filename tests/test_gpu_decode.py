@@ -216,6 +216,29 @@ def test_graph_replay_matches_eager():
     assert torch.equal(a.seqlens, b.seqlens)
 
 
+def test_fused_append_matches_separate_calls():
+    # retopk_decode_step_kv == retopk_append_kv + retopk_decode_step, bit for bit,
+    # eagerly and as a replayed graph, including the K/V caches and lengths
+    w = synth.scaled(synth.WORKLOADS["qwen7b_16k"], steps=24, T_r=8)
+    a = DecodeRun(w, fused=False)
+    arrays = (a.k_host, a.v_host, a.qp_host, a.qd_host)
+    b = DecodeRun(w, arrays=arrays, fused=True)
+    c = DecodeRun(w, arrays=arrays, fused=True)
+    c.capture()
+    for t in range(w.steps):
+        a.step(t)
+        b.step(t)
+        c.replay(t)
+        torch.cuda.synchronize()
+        assert torch.equal(a.out, b.out) and torch.equal(a.out, c.out), t
+    for x in (b, c):
+        sa, sx = a.ctx.retopk_export_state(), x.ctx.retopk_export_state()
+        for key in sa:
+            assert np.array_equal(sa[key], sx[key]), key
+        assert torch.equal(a.seqlens, x.seqlens)
+        assert torch.equal(a.k_cache, x.k_cache) and torch.equal(a.v_cache, x.v_cache)
+
+
 def test_state_round_trip_and_status_bits():
     w = synth.scaled(synth.WORKLOADS["qwen7b_16k"], L0=2048, steps=4)
     dr = DecodeRun(w)
@@ -238,6 +261,10 @@ def test_state_round_trip_and_status_bits():
     # appending to a full cache is reported and leaves the length unchanged
     dr.seqlens.fill_(dr.max_len)
     dr.ctx.retopk_append_kv(dr.k_new[0], dr.v_new[0], dr.k_cache, dr.v_cache, dr.seqlens)
+    assert dr.ctx.retopk_get_status(clear=True) & 0x2
+    assert (dr.seqlens.cpu() == dr.max_len).all()
+    # ... also through the fused append + decode step
+    dr.ctx.retopk_decode_step_kv(dr.k_new[0], dr.v_new[0], dr.q_dec[2], dr.k_cache, dr.v_cache, dr.seqlens, dr.out)
     assert dr.ctx.retopk_get_status() & 0x2
     assert (dr.seqlens.cpu() == dr.max_len).all()
     # malformed state buffers are refused on the host

@@ -384,6 +384,28 @@ int retopk_append_kv(retopk_ctx *ctx, const retopk_bf16 *k_new, const retopk_bf1
                          [&] { return launch_append(ctx->w, k_new, v_new, k_cache, v_cache, d_seqlens, st); }));
 }
 
+namespace {
+
+// decide (with the append when k_new != null) -> scan -> finish
+int decode_step(retopk_ctx *ctx, const retopk_bf16 *k_new, const retopk_bf16 *v_new, const retopk_bf16 *q,
+                retopk_bf16 *k_cache, retopk_bf16 *v_cache, int32_t *d_seqlens, retopk_bf16 *out,
+                cudaStream_t st)
+{
+    const Work &w = ctx->w;
+    QSrc qs{q, (long long)w.Hq * kD, kD};
+    int e;
+    if ((e = cuda_rc(timed(RETOPK_PROF_DECIDE, st, [&] {
+             return launch_decide(w, q, k_new, v_new, k_cache, v_cache, d_seqlens, st);
+         }))))
+        return e;
+    if ((e = run_scan(w, qs, k_cache, d_seqlens, 0, st)))
+        return e;
+    return cuda_rc(timed(RETOPK_PROF_FINISH, st,
+                         [&] { return launch_finish(w, q, k_cache, v_cache, d_seqlens, out, st); }));
+}
+
+}  // namespace
+
 int retopk_decode_step(retopk_ctx *ctx, const retopk_bf16 *q, const retopk_bf16 *k_cache,
                        const retopk_bf16 *v_cache, const int32_t *d_seqlens, retopk_bf16 *out,
                        void *stream)
@@ -392,18 +414,24 @@ int retopk_decode_step(retopk_ctx *ctx, const retopk_bf16 *q, const retopk_bf16 
         return RETOPK_ERR_INVALID;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
         return RETOPK_ERR_ALIGN;
-    cudaStream_t st = (cudaStream_t)stream;
-    const Work &w = ctx->w;
-    QSrc qs{q, (long long)w.Hq * kD, kD};
-    int e;
     // path decision (Eqs. (6), (7), (13)); the scan of the groups with an exact
-    // head; every head's back end in one launch
-    if ((e = cuda_rc(timed(RETOPK_PROF_DECIDE, st, [&] { return launch_decide(w, q, d_seqlens, st); }))))
-        return e;
-    if ((e = run_scan(w, qs, k_cache, d_seqlens, 0, st)))
-        return e;
-    return cuda_rc(timed(RETOPK_PROF_FINISH, st,
-                         [&] { return launch_finish(w, q, k_cache, v_cache, d_seqlens, out, st); }));
+    // head; every head's back end in one launch.  Nothing is written through
+    // the cache or length pointers without an append.
+    return decode_step(ctx, nullptr, nullptr, q, const_cast<retopk_bf16 *>(k_cache),
+                       const_cast<retopk_bf16 *>(v_cache), const_cast<int32_t *>(d_seqlens), out,
+                       (cudaStream_t)stream);
+}
+
+int retopk_decode_step_kv(retopk_ctx *ctx, const retopk_bf16 *k_new, const retopk_bf16 *v_new,
+                          const retopk_bf16 *q, retopk_bf16 *k_cache, retopk_bf16 *v_cache,
+                          int32_t *d_seqlens, retopk_bf16 *out, void *stream)
+{
+    if (!ctx || !k_new || !v_new || !q || !k_cache || !v_cache || !d_seqlens || !out)
+        return RETOPK_ERR_INVALID;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned16(out))
+        return RETOPK_ERR_ALIGN;
+    return decode_step(ctx, k_new, v_new, q, k_cache, v_cache, d_seqlens, out, (cudaStream_t)stream);
 }
 
 int retopk_get_diagnostics(retopk_ctx *ctx, int32_t *path, float *rho_max, int32_t *topR, int32_t *M,

@@ -15,6 +15,15 @@ namespace retopk {
 constexpr int kDecideThreads = 256;
 static_assert(kMaxC <= kDecideThreads, "one cache entry per thread");
 
+struct DecideArgs {
+    Work w;
+    const uint16_t *q;
+    // the token's K/V rows when the append is fused into this launch (else null)
+    const uint16_t *k_new, *v_new;
+    uint16_t *k_cache, *v_cache;
+    int32_t *seqlens;
+};
+
 struct DecideShared {
     float qf[kD];
     float dot[kMaxC];      // by slot
@@ -25,15 +34,34 @@ struct DecideShared {
 };
 
 // Eqs. (6), (7), (13) for one (sequence, query head) per CTA.
-__global__ void __launch_bounds__(kDecideThreads) decide_kernel(ReuseArgs a)
+__global__ void __launch_bounds__(kDecideThreads) decide_kernel(DecideArgs a)
 {
     __shared__ DecideShared sh;
-    pdl_wait();      // the appended row and length, the previous step's cache update
+    pdl_wait();      // the previous step is done with the caches, lengths and ring
     pdl_trigger();   // the scan may set up while the decision runs
     const Work &w = a.w;
     const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = bh / w.Hq;
-    const int L = seq_len(a.seqlens, b, 0, w.max_len);
+    if (a.k_new && bh % w.Hq == 0) {
+        // the fused append: head 0's CTA writes sequence b's new K/V rows at
+        // row L and sets L += 1 (no other CTA of this launch reads L)
+        const int L = a.seqlens[b];
+        if (L >= w.max_len) {
+            if (tid == 0)
+                atomicOr(w.status, RETOPK_STATUS_KV_FULL);
+        } else {
+            constexpr int kPer = kD / 8;   // uint4 per row
+            for (int i = tid; i < 2 * w.Hkv * kPer; i += kDecideThreads) {
+                const int which = i / (w.Hkv * kPer), r = i % (w.Hkv * kPer), hk = r / kPer, c = r % kPer;
+                const uint4 *src = reinterpret_cast<const uint4 *>((which ? a.v_new : a.k_new) + ((size_t)b * w.Hkv + hk) * kD);
+                uint4 *dst = reinterpret_cast<uint4 *>((which ? a.v_cache : a.k_cache) +
+                                                       (((size_t)b * w.Hkv + hk) * w.max_len + L) * kD);
+                dst[c] = src[c];
+            }
+            if (tid == 0)
+                a.seqlens[b] = L + 1;
+        }
+    }
     const int *sq = w.seq + b * SEQ_WORDS;
     const int head = sq[SEQ_HEAD], count = sq[SEQ_COUNT], done = sq[SEQ_TDEC];
     const int t_dec = done + 1;
@@ -110,14 +138,13 @@ __global__ void __launch_bounds__(kDecideThreads) decide_kernel(ReuseArgs a)
         uint4 *hg = reinterpret_cast<uint4 *>(w.hist + (size_t)bh * kHistBins);
         for (int i = tid; i < kHistBins / 4; i += kDecideThreads)
             hg[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (tid == 0)
-            w.M[bh] = L;
     }
 }
 
-cudaError_t launch_decide(const Work &w, const uint16_t *q, const int32_t *seqlens, cudaStream_t st)
+cudaError_t launch_decide(const Work &w, const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                          uint16_t *k_cache, uint16_t *v_cache, int32_t *seqlens, cudaStream_t st)
 {
-    ReuseArgs a{w, q, nullptr, nullptr, seqlens, nullptr, 1.0f / sqrtf((float)kD)};
+    const DecideArgs a{w, q, k_new, v_new, k_cache, v_cache, seqlens};
     return launch_pdl(decide_kernel, dim3(w.B * w.Hq), dim3(kDecideThreads), 0, st, 1, a);
 }
 

@@ -507,6 +507,8 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
                 w.fifo_sup[e_slot * w.K + jj] = v;
         }
         if (rank == 0 && tid == 0) {
+            if (a.mode == FIN_DECODE)
+                w.M[bh] = L;                       // an exact head "considers" every key
             if (w.support)
                 w.sup_len[bh] = n;
             if (insert)

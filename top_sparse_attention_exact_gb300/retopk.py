@@ -22,7 +22,7 @@ RETOPK_PATH_REUSE, RETOPK_PATH_FALLBACK, RETOPK_PATH_REFRESH = 0, 1, 2
 STATUS_BAD_INDEX, STATUS_KV_FULL, STATUS_NONFINITE = 0x1, 0x2, 0x4
 
 EXPORTED = ("retopk_workspace_bytes", "retopk_create", "retopk_destroy", "retopk_init_cache",
-            "retopk_append_kv", "retopk_decode_step", "retopk_get_diagnostics",
+            "retopk_append_kv", "retopk_decode_step", "retopk_decode_step_kv", "retopk_get_diagnostics",
             "retopk_get_counters", "retopk_state_bytes", "retopk_export_state",
             "retopk_import_state", "retopk_get_status", "retopk_strerror", "retopk_cuda_error_string",
             "exact_topk_workspace_bytes", "exact_topk_attention_step",
@@ -56,6 +56,7 @@ def _declare(lib):
     lib.retopk_init_cache.argtypes = [_P, _P, _P, _P, _P]
     lib.retopk_append_kv.argtypes = [_P, _P, _P, _P, _P, _P, _P]
     lib.retopk_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P]
+    lib.retopk_decode_step_kv.argtypes = [_P] * 9
     lib.retopk_get_diagnostics.argtypes = [_P] + [_P] * 8 + [_P]
     lib.retopk_get_counters.argtypes = [_P, _P, _P]
     lib.retopk_state_bytes.argtypes = [_P]
@@ -227,6 +228,13 @@ class ReTopK:
         _check(load().retopk_decode_step(self.handle, _ptr(_bf16(q)), _ptr(_bf16(k_cache)),
                                          _ptr(_bf16(v_cache)), _ptr(_i32(seqlens)), _ptr(_bf16(out)),
                                          _stream(stream)), "retopk_decode_step")
+        return out
+
+    def retopk_decode_step_kv(self, k_new, v_new, q, k_cache, v_cache, seqlens, out, stream=None):
+        """retopk_append_kv + retopk_decode_step in one fewer launch."""
+        _check(load().retopk_decode_step_kv(self.handle, _ptr(_bf16(k_new)), _ptr(_bf16(v_new)), _ptr(_bf16(q)),
+                                            _ptr(_bf16(k_cache)), _ptr(_bf16(v_cache)), _ptr(_i32(seqlens)),
+                                            _ptr(_bf16(out)), _stream(stream)), "retopk_decode_step_kv")
         return out
 
     # --- inspection -------------------------------------------------------------

@@ -21,8 +21,12 @@ def to_dev(a: np.ndarray, device) -> torch.Tensor:
 
 
 class DecodeRun:
-    def __init__(self, w: synth.Workload, arrays=None, device="cuda", max_len=None):
+    """`fused` runs each step through retopk_decode_step_kv (append folded into
+    the decision kernel); otherwise retopk_append_kv then retopk_decode_step."""
+
+    def __init__(self, w: synth.Workload, arrays=None, device="cuda", max_len=None, fused: bool = True):
         self.w = w
+        self.fused = fused
         self.device = torch.device(device)
         k, v, qp, qd = arrays if arrays is not None else synth.generate(w)
         self.k_host, self.v_host, self.qp_host, self.qd_host = k, v, qp, qd
@@ -48,14 +52,21 @@ class DecodeRun:
     # ---- eager -----------------------------------------------------------
     def step(self, t: int | None = None, stream=None):
         t = self.t if t is None else t
-        self.ctx.retopk_append_kv(self.k_new[t], self.v_new[t], self.k_cache, self.v_cache, self.seqlens, stream)
-        self.ctx.retopk_decode_step(self.q_dec[t], self.k_cache, self.v_cache, self.seqlens, self.out, stream)
+        self._one(self.k_new[t], self.v_new[t], self.q_dec[t], stream)
         self.t = t + 1
         return self.out
 
+    def _one(self, k_new, v_new, q, stream):
+        if self.fused:
+            self.ctx.retopk_decode_step_kv(k_new, v_new, q, self.k_cache, self.v_cache, self.seqlens, self.out,
+                                           stream)
+        else:
+            self.ctx.retopk_append_kv(k_new, v_new, self.k_cache, self.v_cache, self.seqlens, stream)
+            self.ctx.retopk_decode_step(q, self.k_cache, self.v_cache, self.seqlens, self.out, stream)
+
     # ---- CUDA graph: one capture, replayed with per-step staging copies ----
     def capture(self, profiled: bool = False):
-        """Capture append + decode as one graph; `profiled` embeds the library's
+        """Capture one decode step (append included) as a graph; `profiled` embeds the library's
         per-kernel timing events in it (read them with retopk.profile_read)."""
         w = self.w
         self.q_buf = torch.empty((w.B, w.Hq, w.d), dtype=torch.int16, device=self.device)
@@ -70,8 +81,7 @@ class DecodeRun:
         try:
             with torch.cuda.stream(s):
                 with torch.cuda.graph(g, stream=s):
-                    self.ctx.retopk_append_kv(self.k_buf, self.v_buf, self.k_cache, self.v_cache, self.seqlens, s)
-                    self.ctx.retopk_decode_step(self.q_buf, self.k_cache, self.v_cache, self.seqlens, self.out, s)
+                    self._one(self.k_buf, self.v_buf, self.q_buf, s)
         finally:
             if profiled:
                 profile_enable(False)
