@@ -195,16 +195,6 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes
                  : "memory");
 }
 
-// 16-byte asynchronous copy global -> shared through the load path (one per
-// thread and call); cp_async_wait_all() then a block barrier make them visible.
-__device__ __forceinline__ void cp_async16(void *dst, const void *src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src))
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 // 1-D bulk copy global -> shared (TMA), completing on `bar`.  dst, src 16-byte
 // aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)

@@ -54,16 +54,9 @@ static_assert(kSubBins == 256, "second-level digit is 8 bits");
 // partials share one region (they are live in phases 1, 2 and 3)
 constexpr size_t kSelRegionBytes = (size_t)kSliceCap * 4 > (size_t)kSelStageCap * 8 ? (size_t)kSliceCap * 4
                                                                                    : (size_t)kSelStageCap * 8;
-// Region layout after the filter: staging arrays st_idx [0, 32 KiB) and
-// st_key [32 KiB, 64 KiB); with at most kVPreCap final candidates the V rows
-// of a rank's share of them are copied to [kVPreOff, 32 KiB) while the Top-K
-// is selected; the per-warp value partials sit at kRedOff.
-constexpr size_t kVPreOff = 4096;
-constexpr int kVPreRows = (int)((32768 - kVPreOff) / (kD * 2));   // per rank
-constexpr int kVPreCap = kVPreRows * kExactCluster;
-constexpr size_t kRedOff = 40960;
-static_assert(kVPreOff >= (size_t)kVPreCap * 4 && 32768 + (size_t)kVPreCap * 4 <= kRedOff, "staging below the V rows");
-static_assert(kRedOff + (size_t)kSelWarps * kD * 4 <= kSelRegionBytes, "value partials fit the region");
+// the per-warp value partials use the region's start once the staging
+// arrays are dead
+static_assert((size_t)kSelWarps * kD * 4 <= kSelRegionBytes, "value partials fit the region");
 static_assert(kHistBins == 4 * kSelThreads, "one uint4 of histogram per thread");
 
 struct SelArgs {
@@ -88,6 +81,9 @@ struct SelShared {
     alignas(16) uint32_t h2[kSubBins];             // this rank's digit-T1 keys by second-level digit
     alignas(16) uint32_t h2all[kExactCluster][kSubBins];   // every rank's h2 (pushed by the ranks)
     SelectShared sel;
+    int ntie;                                      // final candidates sharing the prefix (T1, T2)
+    unsigned long long tie[32];                    // their composite keys (when at most 32)
+    unsigned long long tie_thr;                    // the rem-th largest of them
     uint32_t kmax;
     float zw[kSelWarps];
     alignas(16) float part_o[kExactCluster][kD];   // rank 0 receives every rank's partial
@@ -183,8 +179,7 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     float *slice = reinterpret_cast<float *>(xs);                          // [kSliceCap], phase 1
     int32_t *st_idx = reinterpret_cast<int32_t *>(xs);                     // [kSelStageCap], phase 2
     uint32_t *st_key = reinterpret_cast<uint32_t *>(st_idx + kSelStageCap);
-    uint16_t *vrows = reinterpret_cast<uint16_t *>(xs + kVPreOff);         // [kVPreRows][kD], phases 2-3
-    float(*red)[kD] = reinterpret_cast<float(*)[kD]>(xs + kRedOff);        // [kSelWarps][kD], phase 3
+    float(*red)[kD] = reinterpret_cast<float(*)[kD]>(xs);                  // [kSelWarps][kD], phase 3
     int32_t *loc_i = reinterpret_cast<int32_t *>(xs + kSelRegionBytes);    // [kLocCap]
     uint32_t *loc_k = reinterpret_cast<uint32_t *>(loc_i + kLocCap);
     const int Kp = (w.K + 3) & ~3;
@@ -195,6 +190,7 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     //         first) while the threshold digit is found from the histogram ---
     if (tid == 0) {
         mbar_init(&sh.bar, 1);
+        sh.ntie = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         sh.kmax = 0u;
         sh.T1 = 0;
@@ -435,35 +431,45 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
         idx = st_idx[j];
         k = st_key[j];
     };
-    // With few final candidates, rank r's 1/kExactCluster of them (in staging
-    // order) get their V rows copied to shared memory now (16-byte asynchronous
-    // copies from every thread) while the Top-K is selected; Eq. (12) then
-    // sums over that share with weight 0 for the candidates outside the
-    // support.
-    const bool vpre = staged && N2 <= kVPreCap && a.mode != FIN_INIT;
-    const int cper = (N2 + kExactCluster - 1) / kExactCluster;
-    const int vc0 = min(N2, rank * cper), vc1 = min(N2, vc0 + cper);
     const uint16_t *vb = a.v + ((size_t)(b * w.Hkv + hk) * w.max_len) * kD;
-    if (vpre) {
-        constexpr int kChunks = kD * 2 / 16;   // 16-byte pieces of a row
-        for (int c = tid; c < (vc1 - vc0) * kChunks; c += kSelThreads) {
-            const int j = vc0 + c / kChunks, part = c % kChunks;
-            cp_async16(vrows + (size_t)(j - vc0) * kD + part * 8, vb + (size_t)st_idx[j] * kD + part * 8);
-        }
-        cp_async_commit();
-    }
     int n;
     unsigned long long thr = 0ull;
     if (staged) {
         // every key above prefix (T1, T2) is in; the need - above2 others come
-        // from the keys with that prefix (a histogram that disagreed with the
-        // scores -- no T2 found -- falls back to the full select)
+        // from the keys with that prefix.  Those few are listed and ranked by
+        // one warp (composite keys are distinct); more than 32 of them take the
+        // radix refinement, and a histogram that disagreed with the scores (no
+        // T2 found) falls back to the full select.
+        const int rem = need - sh.above2;
+        if (N2 > need && sh.above2 >= 0) {
+            for (int j = tid; j < N2; j += kSelThreads) {
+                const uint32_t k = st_key[j];
+                if ((k >> kSub) == p19) {
+                    const int s = atomicAdd(&sh.ntie, 1);
+                    if (s < 32)
+                        sh.tie[s] = key64(k, st_idx[j]);
+                }
+            }
+            __syncthreads();
+            if (sh.ntie <= 32) {
+                if (warp == 0) {
+                    const int nt = sh.ntie;
+                    const unsigned long long mine = lane < nt ? sh.tie[lane] : 0ull;
+                    int rk = 0;   // how many tied keys are larger
+                    for (int i = 0; i < nt; ++i)
+                        rk += sh.tie[i] > mine;
+                    if (lane < nt && rk == rem - 1)
+                        sh.tie_thr = mine;
+                }
+                __syncthreads();
+            }
+        }
         thr =
-            N2 <= need       ? 0ull
-            : sh.above2 >= 0 ? radix_refine<kSelThreads>(N2, need - sh.above2,
-                                                         (unsigned long long)p19 << (32 + kSub), 32 + kSub,
-                                                         get_staged, sh.sel)
-                             : radix_select_threshold<kSelThreads>(N2, need, get_staged, sh.sel);
+            N2 <= need                        ? 0ull
+            : sh.above2 < 0                   ? radix_select_threshold<kSelThreads>(N2, need, get_staged, sh.sel)
+            : sh.ntie <= 32                   ? sh.tie_thr
+                                              : radix_refine<kSelThreads>(N2, rem, (unsigned long long)p19 << (32 + kSub),
+                                                                          32 + kSub, get_staged, sh.sel);
         n = stable_compact<kSelThreads, 4>(N2, thr, get_staged, w.K, sup_i, sup_k, sh.sel.warp_tot);
     } else {
         // more than kSelStageCap final candidates: select among all of them
@@ -521,22 +527,7 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     // ---- 3. this rank's share of the value rows (Eq. (12)) -------------------
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float zsum = 0.f;
-    if (vpre) {
-        cp_async_wait_all();
-        __syncthreads();
-        for (int j = vc0 + warp; j < vc1; j += kSelWarps) {   // warp-uniform
-            const uint32_t k = st_key[j];
-            if (key64(k, st_idx[j]) < thr)
-                continue;                                     // not in the support
-            const float p = expf(key2f(k) - m);
-            const uint2 vv = *reinterpret_cast<const uint2 *>(vrows + (size_t)(j - vc0) * kD + lane * 4);
-            zsum += p;
-            acc[0] += p * bf16lo(vv.x);
-            acc[1] += p * bf16hi(vv.x);
-            acc[2] += p * bf16lo(vv.y);
-            acc[3] += p * bf16hi(vv.y);
-        }
-    } else if (a.mode != FIN_INIT) {   // cache initialisation needs the support only
+    if (a.mode != FIN_INIT) {   // cache initialisation needs the support only
         const int vper = (n + kExactCluster - 1) / kExactCluster;
         const int vs = min(n, rank * vper), ve = min(n, vs + vper);
         value_partial<8>(vb, sup_i, sup_k, vs + warp, ve, kSelWarps, m, acc, zsum);
