@@ -215,8 +215,9 @@ def timed_steps(fn_prepare, fn_step, steps, flush, stream):
     return np.array([a.elapsed_time(b) for a, b in ev])
 
 
-def profiled_steps(fn_prepare, fn_step, steps, flush):
-    """Per-kernel in-graph times (us per step) from the library's event nodes."""
+def profiled_steps(fn_prepare, fn_step, steps, flush, on_step=None):
+    """Per-kernel in-graph times (us per step) from the library's event nodes;
+    on_step(t) runs after each step (outside any timing)."""
     import torch
     from top_sparse_attention_exact_gb300 import retopk
     acc = {}
@@ -229,7 +230,28 @@ def profiled_steps(fn_prepare, fn_step, steps, flush):
         for k, (n, ms) in retopk.profile_read().items():
             if n:
                 acc.setdefault(k, []).append(ms * 1000.0)
+        if on_step:
+            on_step(t)
     return {k: float(np.mean(v)) for k, v in acc.items()}
+
+
+def step_bytes(w, path, M, L):
+    """Algorithmic bytes of one decode step (the survey's byte model): K rows of
+    every KV group with an exact-path head, plus per head the V rows of the
+    support and the cache traffic; a reuse head adds its candidate K rows and
+    the retrieved supports."""
+    row = w.d * 2
+    G = w.Hq // w.Hkv
+    total = 0
+    for b in range(w.B):
+        p = path[b * w.Hq:(b + 1) * w.Hq]
+        groups = {h // G for h in range(w.Hq) if p[h] != 0}
+        total += len(groups) * L * row
+        for h in range(w.Hq):
+            total += w.K * row + w.C * row + row + 4 * w.K            # V rows, cache read, slot write
+            if p[h] == 0:
+                total += int(M[b * w.Hq + h]) * row + 4 * w.R * w.K   # candidate K rows, supports
+    return total
 
 
 def our_arm(args, w, rank, world, dist):
@@ -287,13 +309,33 @@ def our_arm(args, w, rank, world, dist):
     for t in range(Wm):
         dp.replay(t)
     retopk.profile_read()
-    kern_decode = profiled_steps(dp.stage, lambda t: dp.graph.replay(), timed_t, flush)
+    step_info = {}
+
+    def record_step(t):
+        d = dp.ctx.retopk_get_diagnostics()
+        step_info[t] = (d["path"].copy(), d["M"].copy())
+
+    kern_decode = profiled_steps(dp.stage, lambda t: dp.graph.replay(), timed_t, flush, record_step)
     retopk.profile_reset()
     exp = ExactRun(dp)
     exp.capture(profiled=True)
     kern_exact = profiled_steps(lambda t: None, exp.replay, timed_t, flush)
     retopk.profile_reset()
     del dp, exp
+    # the same trajectory as the clean run (bit-identical replays): bucket the
+    # clean step times by path mix, and the byte roofline of each step
+    buckets, fracs, reuse_fracs = {}, [], []
+    peak0, _ = measured_peak()
+    for i, t in enumerate(timed_t):
+        pth, Mh = step_info[t]
+        kind = "refresh" if (pth == 2).all() else ("any_exact" if (pth != 0).any() else "all_reuse")
+        buckets.setdefault(kind, []).append(step_ms[i] * 1000.0)
+        gbs = step_bytes(wr, pth, Mh, wr.L0 + t + 1) / (step_ms[i] * 1e-3) / 1e9
+        fracs.append(gbs / peak0)
+        if kind == "all_reuse":
+            reuse_fracs.append(gbs / peak0)
+    path_mix_us = {k: {"steps": len(v), "mean": float(np.mean(v)), "median": float(np.median(v))}
+                   for k, v in sorted(buckets.items())}
     mean_L = float(np.mean([wr.L0 + t + 1 for t in timed_t]))
     scan_bytes = wr.B * wr.Hkv * mean_L * wr.d * 2            # every K row once per GQA group
     scan_us = kern_exact["scan"]
@@ -371,6 +413,11 @@ def our_arm(args, w, rank, world, dist):
                    "refresh_share": mix["refresh"] / head_steps,
                    "mean_candidates": (c1["sum_M"] - c0["sum_M"]) / max(1, mix["reuse"]),
                    "step_us_p50": float(np.median(step_ms) * 1000), "step_us_p90": float(np.percentile(step_ms, 90) * 1000),
+                   "step_us_by_path_mix": path_mix_us,
+                   "step_byte_roofline_frac": {"mean_all_steps": float(np.mean(fracs)),
+                                               "mean_all_reuse_steps": float(np.mean(reuse_fracs)) if reuse_fracs else None,
+                                               "peak_gbs": peak0,
+                                               "bytes": "survey byte model: scanned groups' K rows + per head V rows, cache read/write, reuse candidates and supports"},
                    "kernel_us_per_step_retopk": kern_decode, "kernel_us_per_step_exact": kern_exact,
                    "wall_s_timed_loop": wall},
         "roofline": {"kernel": "scan_kernel (full-history QK + first radix digit), exact step", "bound": "hbm",
