@@ -200,6 +200,20 @@ def test_refresh_every_step_and_always_reuse():
         assert (dr.ctx.retopk_get_diagnostics()["path"] == 0).all()
 
 
+def test_reuse_select_with_heavy_score_ties():
+    # keys drawn from 3 distinct rows (scores take 3 values per query): the
+    # reranked candidates tie in large groups, so the reuse path's Top-K
+    # resolves them by index beyond the warp-ranked case
+    w = synth.scaled(synth.WORKLOADS["tiny_1h_2k"], steps=12, tau=-1.0, T_r=0)
+    k, v, qp, qd = synth.generate(w)
+    rng = np.random.default_rng(11)
+    rows = synth.random_bf16(rng, (3, w.d))
+    k = rows[rng.integers(0, 3, size=k.shape[2])][None, None].copy()
+    dr, errs, agg, paths = run_checked(w, arrays=(k, v, qp, qd))
+    assert not errs, "\n".join(errs[:20])
+    assert (np.concatenate(paths) == 0).all()
+
+
 def test_graph_replay_matches_eager():
     w = synth.scaled(synth.WORKLOADS["qwen7b_16k"], steps=40, T_r=16)
     a = DecodeRun(w)
