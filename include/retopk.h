@@ -223,7 +223,7 @@ int exact_topk_attention_step(const retopk_bf16 *q, const retopk_bf16 *k_cache,
  * allocates nothing (no cudaMalloc / cudaFree, no allocating library call).
  *   - Sizes whose workspace (exact_topk_workspace_bytes) exceeds 16 MiB are
  *     rejected with RETOPK_ERR_SCRATCH before anything is launched (at
- *     Hq = 28, Hkv = 4, K = 512 and B = 1 that allows max_len <= 48960).
+ *     Hq = 28, Hkv = 4, K = 512 and B = 1 that allows max_len <= 49024).
  *   - The array is shared by every call in the process and keeps the last
  *     call's contents; each call clears what must start at zero.  Calls that
  *     overlap on the GPU (other streams, other threads) race on it.

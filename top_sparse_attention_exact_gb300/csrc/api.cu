@@ -82,12 +82,12 @@ int ensure_configured()
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
-int n_filter_for(int) { return kExactCluster; }
-
-int cand_stride_for(int max_len, int n_filter, int RKW)
+// Per-head capacity of the candidate arrays: the kExactCluster segments of an
+// exact head (each a multiple of 16 entries) or a reuse head's A_t.
+int cand_stride_for(int max_len, int RKW)
 {
-    const int seg = (((max_len + n_filter - 1) / n_filter) + 15) & ~15;
-    const int s = std::max(seg * n_filter, RKW);
+    const int seg = (((max_len + kExactCluster - 1) / kExactCluster) + 15) & ~15;
+    const int s = std::max(seg * kExactCluster, RKW);
     return (s + 63) & ~63;
 }
 
@@ -107,9 +107,8 @@ size_t plan(const retopk_config &c, bool stateful, Work *w, char *base)
     x.R = c.R;
     x.T_r = c.T_r;
     x.tau = c.tau;
-    x.n_filter = n_filter_for(c.max_len);
     const int RKW = stateful ? c.R * c.K + c.W : 0;
-    x.cand_stride = cand_stride_for(c.max_len, x.n_filter, RKW);
+    x.cand_stride = cand_stride_for(c.max_len, RKW);
     x.sc_stride = (c.max_len + 15) & ~15;
     const size_t BH = (size_t)c.batch * c.n_q_heads;
     Layout L;
@@ -128,7 +127,6 @@ size_t plan(const retopk_config &c, bool stateful, Work *w, char *base)
     const size_t o_M = L.add(BH * 4);
     const size_t o_ci = L.add(BH * x.cand_stride * 4);
     const size_t o_ck = L.add(BH * x.cand_stride * 4);
-    const size_t o_sg = L.add(BH * x.n_filter * 4);
     const size_t o_sc = L.add(BH * (size_t)x.sc_stride * 4);
     const size_t o_h = L.add(BH * kHistBins * 4);
     const size_t o_sup = L.add(BH * c.K * 4);
@@ -150,7 +148,6 @@ size_t plan(const retopk_config &c, bool stateful, Work *w, char *base)
         x.M = (int32_t *)(base + o_M);
         x.cand_idx = (int32_t *)(base + o_ci);
         x.cand_key = (uint32_t *)(base + o_ck);
-        x.seg_count = (int32_t *)(base + o_sg);
         x.scores = (float *)(base + o_sc);
         x.hist = (uint32_t *)(base + o_h);
         x.support = (int32_t *)(base + o_sup);

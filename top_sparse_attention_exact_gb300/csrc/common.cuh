@@ -33,7 +33,6 @@ struct Work {
     int B, Hq, Hkv, G, max_len, K, C, W, R, T_r;
     float tau;
     int cand_stride;   // per-head capacity of cand_idx / cand_key
-    int n_filter;      // candidate segments per exact head (= kExactCluster)
     int n_scan;        // scan CTAs per (b, h_kv)
     int sc_stride;     // row stride of `scores` (max_len rounded up to 16)
     // query-support cache (decode contexts only)
@@ -50,7 +49,6 @@ struct Work {
     int32_t *M;          // [B*Hq]
     int32_t *cand_idx;   // [B*Hq*cand_stride]
     uint32_t *cand_key;  // [B*Hq*cand_stride]
-    int32_t *seg_count;  // [B*Hq*n_filter]
     float *scores;       // [B*Hq*sc_stride]
     uint32_t *hist;      // [B*Hq*kHistBins]
     int32_t *support;    // [B*Hq*K]
@@ -185,14 +183,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.attrs = attr;
     cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
-}
-
-// L2 prefetch of [src, src + bytes) by the bulk-copy engine (no completion to
-// wait for).  src 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
-                 : "memory");
 }
 
 // 1-D bulk copy global -> shared (TMA), completing on `bar`.  dst, src 16-byte
