@@ -235,6 +235,60 @@ def profiled_steps(fn_prepare, fn_step, steps, flush, on_step=None):
     return {k: float(np.mean(v)) for k, v in acc.items()}
 
 
+def fidelity_pass(w, arrays, dev, n_steps):
+    """Exact shadow over the first n_steps decode steps (untimed): after each
+    ReTopK step the stateless exact step on the same query and caches gives
+    the Exact Top-K support S_t and output; the library's fidelity kernel
+    scores the step's support against it (the paper's "Attention-support
+    fidelity" criterion), and Eq. (2)'s overlap with the most similar cached
+    query and Eq. (3)'s coverage by the R retrieved supports are taken from
+    the exact supports of the steps those cache entries came from."""
+    import torch
+    from top_sparse_attention_exact_gb300.runner import DecodeRun, ExactRun
+    dr = DecodeRun(w, arrays=arrays, device=dev)
+    ex = ExactRun(dr)
+    hist, rows = [], []
+    for s in range(n_steps):
+        dr.step(s)
+        ex.step(dr.q_dec[s])
+        m = dr.ctx.retopk_fidelity(dr.q_dec[s], dr.k_cache, ex.idx, ex.out, dr.out).cpu().numpy().reshape(-1, 4)
+        d = dr.ctx.retopk_get_diagnostics()
+        S = ex.idx.cpu().numpy().reshape(w.B * w.Hq, w.K)
+        hist.append([set(x[x >= 0].tolist()) for x in S])
+        cov = np.full(w.B * w.Hq, np.nan)
+        ovl = np.full(w.B * w.Hq, np.nan)
+        if s >= w.C:   # every cache entry came from a decode step of this pass
+            for bh in range(w.B * w.Hq):
+                pos = [c for c in d["topR"][bh] if c >= 0]
+                steps = [s - w.C + c for c in pos]
+                if not steps:
+                    continue
+                St = hist[s][bh]
+                U = set().union(*(hist[j][bh] for j in steps))
+                cov[bh] = len(St & U) / max(1, len(St))
+                ovl[bh] = len(St & hist[steps[0]][bh]) / max(1, len(St))
+        rows.append((d["path"].copy(), m, cov, ovl))
+    del dr, ex
+    torch.cuda.synchronize()
+
+    def summary(sel):
+        ms = np.concatenate([r[1][sel(r)] for r in rows])
+        cv = np.concatenate([r[2][sel(r)] for r in rows])
+        ov = np.concatenate([r[3][sel(r)] for r in rows])
+        if len(ms) == 0:
+            return None
+        return {"head_steps": int(len(ms)), "support_recall": float(ms[:, 0].mean()),
+                "retained_mass": float(ms[:, 1].mean()), "output_cosine": float(ms[:, 2].mean()),
+                "attention_cosine": float(ms[:, 3].mean()),
+                "coverage_R": float(np.nanmean(cv)) if np.isfinite(cv).any() else None,
+                "overlap_top1": float(np.nanmean(ov)) if np.isfinite(ov).any() else None}
+
+    return {"steps": n_steps, "reuse_path": summary(lambda r: r[0] == 0),
+            "all_heads": summary(lambda r: np.ones_like(r[0], dtype=bool)),
+            "how": "exact shadow (stateless exact step on the same q and caches) after each decode step; "
+                   "retopk_fidelity on the GPU; coverage/overlap from the shadow's exact supports"}
+
+
 def step_bytes(w, path, M, L):
     """Algorithmic bytes of one decode step (the survey's byte model): K rows of
     every KV group with an exact-path head, plus per head the V rows of the
@@ -350,6 +404,9 @@ def our_arm(args, w, rank, world, dist):
     except Exception:
         traffic = None
 
+    # ---- support fidelity against the exact shadow (untimed) -------------------
+    fid = fidelity_pass(wr, arrays, dev, min(wr.steps, args.fidelity_steps)) if args.fidelity_steps > 0 else None
+
     # ---- end to end through the public API with host buffers --------------------
     e2e = None
     if not args.no_e2e:
@@ -418,6 +475,7 @@ def our_arm(args, w, rank, world, dist):
                                                "mean_all_reuse_steps": float(np.mean(reuse_fracs)) if reuse_fracs else None,
                                                "peak_gbs": peak0,
                                                "bytes": "survey byte model: scanned groups' K rows + per head V rows, cache read/write, reuse candidates and supports"},
+                   "fidelity": fid,
                    "kernel_us_per_step_retopk": kern_decode, "kernel_us_per_step_exact": kern_exact,
                    "wall_s_timed_loop": wall},
         "roofline": {"kernel": "scan_kernel (full-history QK + first radix digit), exact step", "bound": "hbm",
@@ -451,6 +509,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fidelity-steps", type=int, default=96)
     args = ap.parse_args()
 
     from top_sparse_attention_exact_gb300 import synth

@@ -235,6 +235,25 @@ int exact_topk_attention_step_noalloc(const retopk_bf16 *q, const retopk_bf16 *k
                                       int B, int Hq, int Hkv, int d, int max_len, int K,
                                       retopk_bf16 *out, int32_t *idx_out, void *stream);
 
+/* ---- fidelity diagnostics ------------------------------------------------ */
+
+/* Attention-support fidelity of the last decode step (ReTopK paper,
+ * §Experiments "Attention-support fidelity", Figs. 5-6; §Motivation
+ * Eq. (2)): for every (sequence, query head), the support that step used
+ * (its reranked support on the reuse path) against `exact_idx`, the Exact
+ * Top-K support of the same query (e.g. idx_out of exact_topk_attention_step
+ * run on the same q and caches), and the step's output `out` against the
+ * exact output `out_exact`.  Scores are recomputed from q and k_cache (call it
+ * before the caches change).  metrics: device float [B, Hq, 4] =
+ *   [0] support recall |S^ n S| / |S|,
+ *   [1] retained mass: the Exact Top-K softmax mass that falls on S^,
+ *   [2] cosine of the two head outputs,
+ *   [3] cosine of the two attention distributions.
+ * exact_idx: [B, Hq, K] int32 ascending, -1 padded; out / out_exact / q:
+ * [B, Hq, d] bf16.  A diagnostic beside the decode loop, not part of it. */
+int retopk_fidelity(retopk_ctx *ctx, const retopk_bf16 *q, const retopk_bf16 *k_cache, const int32_t *exact_idx,
+                    const retopk_bf16 *out_exact, const retopk_bf16 *out, float *metrics, void *stream);
+
 /* ---- profiling ----------------------------------------------------------- */
 
 /* Kernel classes reported by retopk_profile_read. */

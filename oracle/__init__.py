@@ -67,6 +67,7 @@ def _declare(lib):
     lib.oracle_init_cache.restype = _I
     lib.oracle_decode_step.argtypes = [_P, _P, _P, _L, _I, _I, _I, _I, _I, _I, _I, _I, _I, _D,
                                        _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P]
+    lib.oracle_fidelity.argtypes = [_P, _P, _L, _I, _P, _I, _P, _I, _P, _P, _P]
     lib.oracle_set_threads.argtypes = [_I]
     lib.oracle_get_threads.restype = _I
     return lib
@@ -89,6 +90,21 @@ def _i32(a):
 
 def _f64(a):
     return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def fidelity(q, k, S, Sh, o, oh, lib=None):
+    """Support recall, retained Exact Top-K mass, output cosine and attention-
+    distribution cosine of support Sh (output oh) against the exact support S
+    (output o); supports ascending, -1 entries ignored.  k: [L, d] rows."""
+    lib = lib or load()
+    q, k = _u16(q), _u16(k)
+    S = _i32(np.asarray(S)[np.asarray(S) >= 0])
+    Sh = _i32(np.asarray(Sh)[np.asarray(Sh) >= 0])
+    o, oh = _f64(o), _f64(oh)
+    out = np.zeros(4)
+    lib.oracle_fidelity(_p(q), _p(k), k.shape[-1], q.shape[-1], _p(S), len(S), _p(Sh), len(Sh), _p(o), _p(oh),
+                        _p(out))
+    return out
 
 
 def set_threads(n: int) -> None:

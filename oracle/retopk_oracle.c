@@ -415,6 +415,67 @@ void oracle_decode_step(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     seq[2] = t_dec;
 }
 
+/* Attention-support fidelity of a reuse support against the exact one
+ * (ReTopK paper, §Experiments "Attention-support fidelity" with Figs. 5-6,
+ * and §Motivation Eqs. (2)-(3) for the overlap of two supports).  S (nS keys)
+ * is the Exact Top-K support of q, Sh (nh keys) the support being judged;
+ * both ascending.  Scores are recomputed from q and the K rows; p and ph are
+ * the softmax distributions over S and Sh.  out[0] = |Sh n S| / nS (support
+ * recall, Eq. (2)'s overlap with nS = K), out[1] = sum of p over Sh n S (the
+ * Exact Top-K attention mass the support retains), out[2] = cosine of the two
+ * head outputs oh and o (d values each), out[3] = cosine of the two
+ * attention distributions (sum over Sh n S of p ph / (|p| |ph|)). */
+void oracle_fidelity(const uint16_t *q, const uint16_t *k, int64_t ld, int d,
+                     const int32_t *S, int nS, const int32_t *Sh, int nh,
+                     const double *o, const double *oh, double *out)
+{
+    double *eS = (double *)malloc(sizeof(double) * (nS > 0 ? nS : 1));
+    double *eh = (double *)malloc(sizeof(double) * (nh > 0 ? nh : 1));
+    oracle_scores(q, k, ld, S, nS, d, eS);
+    oracle_scores(q, k, ld, Sh, nh, d, eh);
+    double mS = -INFINITY, mh = -INFINITY, ZS = 0.0, Zh = 0.0, p2 = 0.0, ph2 = 0.0;
+    for (int i = 0; i < nS; ++i)
+        mS = fmax(mS, eS[i]);
+    for (int i = 0; i < nh; ++i)
+        mh = fmax(mh, eh[i]);
+    for (int i = 0; i < nS; ++i)
+        ZS += exp(eS[i] - mS);
+    for (int i = 0; i < nh; ++i)
+        Zh += exp(eh[i] - mh);
+    for (int i = 0; i < nS; ++i)
+        p2 += (exp(eS[i] - mS) / ZS) * (exp(eS[i] - mS) / ZS);
+    for (int i = 0; i < nh; ++i)
+        ph2 += (exp(eh[i] - mh) / Zh) * (exp(eh[i] - mh) / Zh);
+    int common = 0;
+    double mass = 0.0, cross = 0.0;
+    for (int a = 0, b = 0; a < nS && b < nh;) {   /* both ascending: merge */
+        if (S[a] < Sh[b]) {
+            ++a;
+        } else if (Sh[b] < S[a]) {
+            ++b;
+        } else {
+            const double p = exp(eS[a] - mS) / ZS, ph = exp(eh[b] - mh) / Zh;
+            ++common;
+            mass += p;
+            cross += p * ph;
+            ++a;
+            ++b;
+        }
+    }
+    double oo = 0.0, hh = 0.0, oh2 = 0.0;
+    for (int c = 0; c < d; ++c) {
+        oo += o[c] * o[c];
+        hh += oh[c] * oh[c];
+        oh2 += o[c] * oh[c];
+    }
+    out[0] = nS > 0 ? (double)common / nS : 1.0;
+    out[1] = mass;
+    out[2] = (oo > 0.0 && hh > 0.0) ? oh2 / (sqrt(oo) * sqrt(hh)) : 0.0;
+    out[3] = (p2 > 0.0 && ph2 > 0.0) ? cross / (sqrt(p2) * sqrt(ph2)) : 0.0;
+    free(eS);
+    free(eh);
+}
+
 void oracle_set_threads(int n)
 {
 #ifdef _OPENMP

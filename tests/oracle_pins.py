@@ -321,8 +321,45 @@ def pin_fifo_contents(lib):
             assert sup.tolist() == res[t]["sup"][h, :res[t]["sup_len"][h]].tolist()
 
 
+def pin_fidelity(lib):
+    """Support recall, retained mass and the two cosines of the fidelity
+    criterion (§Experiments "Attention-support fidelity"; Eq. (2)): a
+    hand-worked case, scipy's cosine for both cosines, and the invariants of
+    identical and disjoint supports."""
+    from scipy.spatial.distance import cosine
+    d = 4
+    q = _bf([2, 0, 0, 0])
+    # scores q.k / sqrt(4): 1, 2, 0, -1
+    k = _bf([[1, 0, 0, 0], [2, 0, 0, 0], [0, 0, 0, 0], [-1, 0, 0, 0]])
+    o = np.array([1.0, 2.0, 0.0, -1.0])
+    oh = np.array([2.0, 1.0, 1.0, 0.0])
+    S, Sh = np.array([0, 1]), np.array([1, 2])
+    m = oracle.fidelity(q, k, S, Sh, o, oh, lib=lib)
+    e = math.e
+    assert m[0] == 0.5, m
+    # p over S = {0, 1} is (1, e) / (1 + e); S^ keeps key 1
+    assert abs(m[1] - e / (1 + e)) < 1e-12, m
+    assert abs(m[2] - (1 - cosine(o, oh))) < 1e-12, m
+    p = np.array([1.0, e, 0.0, 0.0]) / (1 + e)              # over keys 0..3
+    ph = np.array([0.0, e * e, 1.0, 0.0]) / (e * e + 1)       # softmax of (2, 0) on keys 1, 2
+    assert abs(m[3] - (1 - cosine(p, ph))) < 1e-12, m
+    # a shorter judged support: recall still counts against |S|
+    m = oracle.fidelity(q, k, S, np.array([1]), o, oh, lib=lib)
+    assert m[0] == 0.5 and abs(m[1] - e / (1 + e)) < 1e-12, m
+    # identical supports and outputs: everything 1; disjoint supports: 0
+    rng = np.random.default_rng(5)
+    kk = _bf(rng.standard_normal((40, d)))
+    qq = _bf(rng.standard_normal(d))
+    oo = rng.standard_normal(d)
+    full = np.arange(0, 40, 3)
+    m = oracle.fidelity(qq, kk, full, full, oo, oo, lib=lib)
+    assert np.allclose(m, 1.0, rtol=0, atol=1e-12), m
+    m = oracle.fidelity(qq, kk, np.arange(0, 20), np.arange(20, 40), oo, -oo, lib=lib)
+    assert m[0] == 0.0 and m[1] == 0.0 and m[3] == 0.0 and abs(m[2] + 1.0) < 1e-12, m
+
+
 ALL_PINS = [pin_hand_worked_exact, pin_hand_worked_reuse, pin_scores_library_and_closed_form,
             pin_topk_brute_force, pin_softmax_closed_forms, pin_dense_equals_sdpa,
             pin_softmax_merge, pin_recall_closed_forms, pin_candidates_set_union,
             pin_init_cache_causal, pin_degenerate_paths, pin_rerank_recovers_exact,
-            pin_fifo_contents]
+            pin_fifo_contents, pin_fidelity]

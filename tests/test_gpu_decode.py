@@ -214,6 +214,40 @@ def test_reuse_select_with_heavy_score_ties():
     assert (np.concatenate(paths) == 0).all()
 
 
+def test_fidelity_diagnostics_match_oracle():
+    # exact shadow: after each checked decode step, the stateless exact step on
+    # the same query and caches gives S_t and o_t; the library's fidelity
+    # kernel must agree with the oracle's fp64 definitions per head
+    w = synth.scaled(synth.WORKLOADS["qwen7b_16k"], steps=20)
+    dr = DecodeRun(w)
+    ex = ExactRun(dr)
+    seen_reuse = 0
+    for t in range(w.steps):
+        dr.step(t)
+        if t % 4 != 3:
+            continue
+        ex.step(dr.q_dec[t])
+        m = dr.ctx.retopk_fidelity(dr.q_dec[t], dr.k_cache, ex.idx, ex.out, dr.out).cpu().numpy()
+        torch.cuda.synchronize()
+        diag = dr.ctx.retopk_get_diagnostics()
+        S = ex.idx.cpu().numpy()
+        o = synth.bf16_bits_to_f32(ex.out.cpu().numpy().view(np.uint16)).astype(np.float64)
+        oh = synth.bf16_bits_to_f32(dr.out.cpu().numpy().view(np.uint16)).astype(np.float64)
+        L = int(dr.seqlens[0])
+        G = w.Hq // w.Hkv
+        for h in range(w.Hq):
+            ref = oracle.fidelity(dr.qd_host[t, 0, h], dr.k_host[0, h // G, :L], S[0, h], diag["support"][h],
+                                  o[0, h], oh[0, h])
+            got = m[0, h]
+            assert got[0] == ref[0], (t, h, got, ref)
+            assert np.allclose(got[1:], ref[1:], rtol=0, atol=2e-3), (t, h, got, ref)
+            if diag["path"][h] != 0:   # an exact-path head used the exact support
+                assert got[0] == 1.0 and abs(got[1] - 1.0) < 1e-5, (t, h, got)
+            else:
+                seen_reuse += 1
+    assert seen_reuse > 0
+
+
 def test_graph_replay_matches_eager():
     w = synth.scaled(synth.WORKLOADS["qwen7b_16k"], steps=40, T_r=16)
     a = DecodeRun(w)

@@ -42,6 +42,10 @@ MUTANTS = {
                              "        p[c].i = n - 1 - c;\n    }\n    qsort(p, (size_t)n, sizeof(pair_t), cmp_pair);\n"
                              "    for (int c = 0; c < n; ++c) p[c].i = n - 1 - p[c].i;"),
     "reuse_ignores_window": ("    total += L - lo;", "    total += 0; lo = L;"),
+    "fidelity_mass_unnormalised": ("            const double p = exp(eS[a] - mS) / ZS, ph = exp(eh[b] - mh) / Zh;",
+                                   "            const double p = exp(eS[a] - mS), ph = exp(eh[b] - mh) / Zh;"),
+    "fidelity_recall_over_judged": ("    out[0] = nS > 0 ? (double)common / nS : 1.0;",
+                                    "    out[0] = nh > 0 ? (double)common / nh : 1.0;"),
 }
 
 

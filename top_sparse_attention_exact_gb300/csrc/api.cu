@@ -14,6 +14,7 @@ namespace retopk {
 cudaError_t configure_scan();
 cudaError_t configure_select();
 cudaError_t configure_finish();
+cudaError_t configure_fidelity();
 }  // namespace retopk
 
 using namespace retopk;
@@ -76,6 +77,8 @@ int ensure_configured()
             err = configure_select();
         if (err == cudaSuccess)
             err = configure_finish();
+        if (err == cudaSuccess)
+            err = configure_fidelity();
     });
     return cuda_rc(err);
 }
@@ -429,6 +432,18 @@ int retopk_decode_step_kv(retopk_ctx *ctx, const retopk_bf16 *k_new, const retop
         !aligned16(out))
         return RETOPK_ERR_ALIGN;
     return decode_step(ctx, k_new, v_new, q, k_cache, v_cache, d_seqlens, out, (cudaStream_t)stream);
+}
+
+int retopk_fidelity(retopk_ctx *ctx, const retopk_bf16 *q, const retopk_bf16 *k_cache, const int32_t *exact_idx,
+                    const retopk_bf16 *out_exact, const retopk_bf16 *out, float *metrics, void *stream)
+{
+    if (!ctx || !q || !k_cache || !exact_idx || !out_exact || !out || !metrics)
+        return RETOPK_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(out_exact) || !aligned16(out))
+        return RETOPK_ERR_ALIGN;
+    const Work &w = ctx->w;
+    return cuda_rc(launch_fidelity(q, k_cache, exact_idx, w.support, out_exact, out, metrics, w.B, w.Hq, w.Hkv,
+                                   w.max_len, w.K, (cudaStream_t)stream));
 }
 
 int retopk_get_diagnostics(retopk_ctx *ctx, int32_t *path, float *rho_max, int32_t *topR, int32_t *M,

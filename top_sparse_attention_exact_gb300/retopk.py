@@ -27,7 +27,7 @@ EXPORTED = ("retopk_workspace_bytes", "retopk_create", "retopk_destroy", "retopk
             "retopk_import_state", "retopk_get_status", "retopk_strerror", "retopk_cuda_error_string",
             "exact_topk_workspace_bytes", "exact_topk_attention_step",
             "retopk_profile_enable", "retopk_profile_read", "retopk_profile_reset",
-            "retopk_selftest_wait", "exact_topk_attention_step_noalloc")
+            "retopk_selftest_wait", "exact_topk_attention_step_noalloc", "retopk_fidelity")
 
 PROF_KERNELS = ("append", "finish", "scan", "select", "clear", "decide")
 
@@ -57,6 +57,7 @@ def _declare(lib):
     lib.retopk_append_kv.argtypes = [_P, _P, _P, _P, _P, _P, _P]
     lib.retopk_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P]
     lib.retopk_decode_step_kv.argtypes = [_P] * 9
+    lib.retopk_fidelity.argtypes = [_P] * 8
     lib.retopk_get_diagnostics.argtypes = [_P] + [_P] * 8 + [_P]
     lib.retopk_get_counters.argtypes = [_P, _P, _P]
     lib.retopk_state_bytes.argtypes = [_P]
@@ -236,6 +237,16 @@ class ReTopK:
                                             _ptr(_bf16(k_cache)), _ptr(_bf16(v_cache)), _ptr(_i32(seqlens)),
                                             _ptr(_bf16(out)), _stream(stream)), "retopk_decode_step_kv")
         return out
+
+    def retopk_fidelity(self, q, k_cache, exact_idx, out_exact, out, stream=None):
+        """Fidelity of the last decode step's supports/outputs against the exact
+        ones: float32 CUDA tensor [B, Hq, 4] (recall, retained mass, output
+        cosine, attention-distribution cosine)."""
+        m = torch.empty((self.B, self.Hq, 4), dtype=torch.float32, device=q.device)
+        _check(load().retopk_fidelity(self.handle, _ptr(_bf16(q)), _ptr(_bf16(k_cache)), _ptr(_i32(exact_idx)),
+                                      _ptr(_bf16(out_exact)), _ptr(_bf16(out)), _ptr(m), _stream(stream)),
+               "retopk_fidelity")
+        return m
 
     # --- inspection -------------------------------------------------------------
     def retopk_get_diagnostics(self, stream=None) -> dict:
