@@ -50,7 +50,8 @@ def measured_peak():
 
 def workload_desc(w):
     return (f"{w.name}: B={w.B}, Hq={w.Hq}, Hkv={w.Hkv}, d={w.d}, L0={w.L0}, {w.steps} decode steps, "
-            f"K={w.K}, C={w.C}, W={w.W}, R={w.R}, tau={w.tau}, T_r={w.T_r}; topic-mixture keys "
+            f"K={w.K}, C={w.C}, W={w.W}, R={w.R}, tau={w.tau}, T_r={w.T_r}"
+            f"{', recent-R retrieval' if w.recent else ''}; topic-mixture keys "
             f"({w.n_topics} topics, runs of {w.run}), Markov query topics (stay {w.stay})")
 
 
@@ -142,7 +143,8 @@ def run_oracle_steps(w, arrays, state, steps, budget_s=None, b=0):
     k, v, qp, qd = arrays
     done, t0 = 0, time.perf_counter()
     for t in steps:
-        oracle.decode_step(state, qd[t, b], k[b], v[b], w.L0 + t + 1, w.Hkv, w.W, w.R, w.T_r, w.tau)
+        oracle.decode_step(state, qd[t, b], k[b], v[b], w.L0 + t + 1, w.Hkv, w.W, w.R, w.T_r, w.tau,
+                           recent=w.recent)
         done += 1
         if budget_s is not None and time.perf_counter() - t0 > budget_s:
             break
@@ -289,6 +291,57 @@ def fidelity_pass(w, arrays, dev, n_steps):
                    "retopk_fidelity on the GPU; coverage/overlap from the shadow's exact supports"}
 
 
+def layers_pass(w, arrays, dev, n_layers, n_tokens, warm, flush, stream):
+    """ReTopK and Exact Top-K over n_layers independent layer contexts (each
+    with its own KV caches and workspace, the same synthetic inputs), one CUDA
+    graph per token running the layers back to back; the L2 is flushed
+    between tokens only.  Returns ms/token for both."""
+    import torch
+    from top_sparse_attention_exact_gb300.runner import DecodeRun, ExactRun
+    runs = [DecodeRun(w, arrays=arrays, device=dev) for _ in range(n_layers)]
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    q_buf = torch.empty_like(runs[0].q_dec[0])
+    k_buf = torch.empty_like(runs[0].k_new[0])
+    v_buf = torch.empty_like(runs[0].v_new[0])
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for r in runs:
+                r.ctx.retopk_decode_step_kv(k_buf, v_buf, q_buf, r.k_cache, r.v_cache, r.seqlens, r.out, s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+
+    def stage(t):
+        q_buf.copy_(runs[0].q_dec[t])
+        k_buf.copy_(runs[0].k_new[t])
+        v_buf.copy_(runs[0].v_new[t])
+
+    for t in range(warm):
+        stage(t)
+        g.replay()
+    ms = timed_steps(stage, lambda t: g.replay(), range(warm, warm + n_tokens), flush, stream)
+    # the exact path on the same layers, caches and queries
+    exs = [ExactRun(r) for r in runs]
+    ge = torch.cuda.CUDAGraph()
+    q_e = torch.empty_like(runs[0].q_dec[0])
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(ge, stream=s):
+            for e in exs:
+                e.step(q_e, s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    ms_e = timed_steps(lambda t: q_e.copy_(runs[0].q_dec[t]), lambda t: ge.replay(), range(warm, warm + n_tokens),
+                       flush, stream)
+    del runs, exs, g, ge
+    torch.cuda.synchronize()
+    return {"layers": n_layers, "tokens": n_tokens, "retopk_ms_per_token": float(ms.mean()),
+            "exact_ms_per_token": float(ms_e.mean()), "retopk_us_per_layer": float(ms.mean() * 1000 / n_layers),
+            "speedup_vs_exact": float(ms_e.mean() / ms.mean()),
+            "how": "one CUDA graph per token with the layers back to back (programmatic launch overlap "
+                   "between layers), L2 flushed between tokens; independent layer contexts on the same inputs"}
+
+
 def step_bytes(w, path, M, L):
     """Algorithmic bytes of one decode step (the survey's byte model): K rows of
     every KV group with an exact-path head, plus per head the V rows of the
@@ -404,6 +457,10 @@ def our_arm(args, w, rank, world, dist):
     except Exception:
         traffic = None
 
+    # ---- the paper's per-token unit: a stack of layers in one graph -------------
+    layers = (layers_pass(wr, arrays, dev, args.layers, args.layer_tokens, Wm, flush, stream)
+              if args.layers > 0 and rank == 0 else None)
+
     # ---- support fidelity against the exact shadow (untimed) -------------------
     fid = fidelity_pass(wr, arrays, dev, min(wr.steps, args.fidelity_steps)) if args.fidelity_steps > 0 else None
 
@@ -476,6 +533,7 @@ def our_arm(args, w, rank, world, dist):
                                                "peak_gbs": peak0,
                                                "bytes": "survey byte model: scanned groups' K rows + per head V rows, cache read/write, reuse candidates and supports"},
                    "fidelity": fid,
+                   "layer_stack": layers,
                    "kernel_us_per_step_retopk": kern_decode, "kernel_us_per_step_exact": kern_exact,
                    "wall_s_timed_loop": wall},
         "roofline": {"kernel": "scan_kernel (full-history QK + first radix digit), exact step", "bound": "hbm",
@@ -510,10 +568,21 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--fidelity-steps", type=int, default=96)
+    ap.add_argument("--layers", type=int, default=28)
+    ap.add_argument("--set", action="append", default=[], help="override a workload field, e.g. tau=-inf")
+    ap.add_argument("--layer-tokens", type=int, default=64)
     args = ap.parse_args()
 
     from top_sparse_attention_exact_gb300 import synth
     w = synth.WORKLOADS[args.workload]
+    if args.set:   # ablations: --set tau=-inf --set W=0 --set recent=1 ...
+        kw = {}
+        for item in args.set:
+            key, val = item.split("=", 1)
+            cur = getattr(w, key)
+            kw[key] = (val not in ("0", "false", "False")) if isinstance(cur, bool) else type(cur)(float(val))
+        tag = ",".join(args.set)
+        w = synth.scaled(w, name=f"{w.name}[{tag}]", **kw)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     dist = None

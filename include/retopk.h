@@ -80,7 +80,14 @@ typedef struct retopk_config {
     int32_t max_len;      /* rows per (b, h_kv) in the caller's KV cache        */
     int32_t K, C, W, R, T_r;
     float tau;
+    int32_t retrieval;    /* RETOPK_RETRIEVE_SIMILAR (0): the R most similar
+                             cached queries, Eq. (7) -- the method; or
+                             RETOPK_RETRIEVE_RECENT (1): the R most recent
+                             entries, rho_max over them (the paper's Table 3
+                             "recent-R retrieval" ablation)                  */
 } retopk_config;
+#define RETOPK_RETRIEVE_SIMILAR 0
+#define RETOPK_RETRIEVE_RECENT  1
 
 /* ---- context ------------------------------------------------------------ */
 

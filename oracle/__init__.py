@@ -65,7 +65,9 @@ def _declare(lib):
     lib.oracle_exact_step.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _L, _I, _P, _P, _P, _P]
     lib.oracle_init_cache.argtypes = [_P, _P, _L, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]
     lib.oracle_init_cache.restype = _I
-    lib.oracle_decode_step.argtypes = [_P, _P, _P, _L, _I, _I, _I, _I, _I, _I, _I, _I, _I, _D,
+    lib.oracle_recall_recent.argtypes = [_P, _P, _I, _I, _I, _P, _P]
+    lib.oracle_recall_recent.restype = _D
+    lib.oracle_decode_step.argtypes = [_P, _P, _P, _L, _I, _I, _I, _I, _I, _I, _I, _I, _I, _D, _I,
                                        _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P]
     lib.oracle_fidelity.argtypes = [_P, _P, _L, _I, _P, _I, _P, _I, _P, _P, _P]
     lib.oracle_set_threads.argtypes = [_I]
@@ -277,7 +279,7 @@ def init_cache(q_prompt, k, L0, Hq, Hkv, K, C, lib=None) -> CacheState:
     return st
 
 
-def decode_step(st: CacheState, q, k, v, L, Hkv, W, R, T_r, tau, lib=None) -> dict:
+def decode_step(st: CacheState, q, k, v, L, Hkv, W, R, T_r, tau, lib=None, recent: bool = False) -> dict:
     """One ReTopK decode step for one sequence; updates `st` in place.
 
     q [Hq,d]; k, v [Hkv,max_len,d]; L = keys including the current one.
@@ -293,7 +295,7 @@ def decode_step(st: CacheState, q, k, v, L, Hkv, W, R, T_r, tau, lib=None) -> di
         sup=np.empty((Hq, K), np.int32), sup_len=np.empty(Hq, np.int32),
         kth=np.empty(Hq, np.float64), out=np.empty((Hq, d), np.float64))
     lib.oracle_decode_step(_p(q), _p(k), _p(v), k.shape[1], int(L), Hq, Hkv, d, K, C, int(W),
-                           int(R), int(T_r), float(tau), _p(st.fq), _p(st.fsup), _p(st.flen),
+                           int(R), int(T_r), float(tau), int(bool(recent)), _p(st.fq), _p(st.fsup), _p(st.flen),
                            _p(st.seq), _p(r["path"]), _p(r["rho"]), _p(r["rho_max"]),
                            _p(r["topR"]), _p(r["cand"]), cap, _p(r["M"]), _p(r["sup"]),
                            _p(r["sup_len"]), _p(r["kth"]), _p(r["out"]))

@@ -327,9 +327,30 @@ int oracle_init_cache(const uint16_t *qp, const uint16_t *k, int64_t max_len, in
 /*   sup[h*K+j], sup_len[h]: the selected support, ascending (-1 padded)      */
 /*   kth[h]     score of the K-th ranked key of the support                   */
 /*   out[h*d+c] Eq. (12) output                                               */
+/* The ablation the paper's Table 3 calls "recent-R retrieval": the R most
+ * recent live entries (newest first) instead of the R most similar, with
+ * rho_max taken over them.  rho: every entry's cosine, as for Eq. (6). */
+double oracle_recall_recent(const uint16_t *q, const uint16_t *const *cached, int n, int d,
+                            int R, double *rho, int32_t *topR)
+{
+    int32_t *tmp = (int32_t *)malloc(sizeof(int32_t) * (size_t)(R > 0 ? R : 1));
+    oracle_recall(q, cached, n, d, R, rho, tmp);   /* the cosines */
+    free(tmp);
+    int m = n < R ? n : R;
+    double rmax = -INFINITY;
+    for (int r = 0; r < m; ++r) {
+        topR[r] = n - 1 - r;
+        if (rho[n - 1 - r] > rmax)
+            rmax = rho[n - 1 - r];
+    }
+    for (int r = m; r < R; ++r)
+        topR[r] = -1;
+    return rmax;
+}
+
 void oracle_decode_step(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                         int64_t max_len, int L, int Hq, int Hkv, int d,
-                        int K, int C, int W, int R, int T_r, double tau,
+                        int K, int C, int W, int R, int T_r, double tau, int recent,
                         uint16_t *fq, int32_t *fsup, int32_t *flen, int32_t *seq,
                         int32_t *path, double *rho, double *rho_max, int32_t *topR,
                         int32_t *cand, int cap, int32_t *M,
@@ -356,7 +377,8 @@ void oracle_decode_step(const uint16_t *q, const uint16_t *k, const uint16_t *v,
         }
         for (int c = 0; c < C; ++c)
             rho[(int64_t)h * C + c] = NAN;
-        rho_max[h] = oracle_recall(qh, cq, count, d, R, rho + (int64_t)h * C, topR + (int64_t)h * R);
+        rho_max[h] = (recent ? oracle_recall_recent : oracle_recall)(qh, cq, count, d, R, rho + (int64_t)h * C,
+                                                                  topR + (int64_t)h * R);
         /* Eq. (13) */
         int p = refresh ? 2 : (rho_max[h] < tau || isnan(rho_max[h])) ? 1 : 0;
         path[h] = p;

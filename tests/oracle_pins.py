@@ -321,6 +321,27 @@ def pin_fifo_contents(lib):
             assert sup.tolist() == res[t]["sup"][h, :res[t]["sup_len"][h]].tolist()
 
 
+def pin_recent_retrieval(lib):
+    """The "recent-R retrieval" ablation (Table 3): the R newest live entries,
+    newest first, with rho_max over them only -- checked on cached queries
+    whose cosines with q are known in closed form (parallel, antiparallel,
+    orthogonal), the most similar one being the oldest."""
+    q = _bf([1, 0, 0, 0])
+    cached = _bf([[3, 0, 0, 0],      # cosine  1, oldest
+                  [0, 1, 0, 0],      # 0
+                  [-2, 0, 0, 0],     # -1
+                  [0, 0, 5, 0]])     # 0, newest
+    rho = np.empty(4)
+    top = np.empty(2, dtype=np.int32)
+    ptrs = (__import__("ctypes").c_void_p * 4)(*[cached[c].ctypes.data for c in range(4)])
+    rmax = lib.oracle_recall_recent(q.ctypes.data, ptrs, 4, 4, 2, rho.ctypes.data, top.ctypes.data)
+    assert top.tolist() == [3, 2], top
+    assert rmax == 0.0 and np.allclose(rho, [1.0, 0.0, -1.0, 0.0], rtol=0, atol=1e-15), (rmax, rho)
+    top3 = np.empty(5, dtype=np.int32)
+    rmax = lib.oracle_recall_recent(q.ctypes.data, ptrs, 4, 4, 5, rho.ctypes.data, top3.ctypes.data)
+    assert top3.tolist() == [3, 2, 1, 0, -1] and rmax == 1.0, (top3, rmax)
+
+
 def pin_fidelity(lib):
     """Support recall, retained mass and the two cosines of the fidelity
     criterion (§Experiments "Attention-support fidelity"; Eq. (2)): a
@@ -362,4 +383,4 @@ ALL_PINS = [pin_hand_worked_exact, pin_hand_worked_reuse, pin_scores_library_and
             pin_topk_brute_force, pin_softmax_closed_forms, pin_dense_equals_sdpa,
             pin_softmax_merge, pin_recall_closed_forms, pin_candidates_set_union,
             pin_init_cache_causal, pin_degenerate_paths, pin_rerank_recovers_exact,
-            pin_fifo_contents, pin_fidelity]
+            pin_fifo_contents, pin_fidelity, pin_recent_retrieval]

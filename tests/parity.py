@@ -109,7 +109,8 @@ def compare_decode_step(pre: dict, post: dict, diag: dict, q_t, k, v, L, w, gpu_
     stats = dict(path_band=0, topR_band=0, swaps=0, heads=0)
     for b in range(B):
         cs = oracle_state_from_gpu(pre, b, K)
-        r = oracle.decode_step(cs, q_t[b], k[b], v[b], int(L[b]), w.Hkv, w.W, R, w.T_r, w.tau)
+        r = oracle.decode_step(cs, q_t[b], k[b], v[b], int(L[b]), w.Hkv, w.W, R, w.T_r, w.tau,
+                               recent=getattr(w, "recent", False))
         for h in range(Hq):
             bh = b * Hq + h
             stats["heads"] += 1

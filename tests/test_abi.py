@@ -42,6 +42,7 @@ def test_config_validation_without_gpu(lib):
         retopk.retopk_config(1, 28, 4, 128, 1024, 512, 32, -1, 4, 128, 0.85),   # W
         retopk.retopk_config(1, 28, 4, 128, 1 << 21, 512, 32, 32, 4, 128, 0.85),  # max_len
         retopk.retopk_config(1, 28, 4, 128, 1024, 512, 32, 32, 4, 128, float("nan")),
+        retopk.retopk_config(1, 28, 4, 128, 1024, 512, 32, 32, 4, 128, 0.85, 2),   # retrieval mode
     ]
     for c in bad:
         assert lib.retopk_workspace_bytes(ctypes.byref(c)) == 0

@@ -69,7 +69,8 @@ def test_tiny_free_running_matches_oracle():
             assert np.array_equal(g0["fifo_sup"][0, h, c, :n], st.fsup[h, c, :n])
     for t in range(w.steps):
         dr.step(t)
-        r = oracle.decode_step(st, qd[t, 0], k[0], v[0], w.L0 + t + 1, w.Hkv, w.W, w.R, w.T_r, w.tau)
+        r = oracle.decode_step(st, qd[t, 0], k[0], v[0], w.L0 + t + 1, w.Hkv, w.W, w.R, w.T_r, w.tau,
+                               recent=w.recent)
         diag = dr.ctx.retopk_get_diagnostics()
         assert diag["path"].tolist() == r["path"].tolist(), t
         assert diag["support"][0, :diag["sup_len"][0]].tolist() == r["sup"][0, :r["sup_len"][0]].tolist(), t
@@ -212,6 +213,15 @@ def test_reuse_select_with_heavy_score_ties():
     dr, errs, agg, paths = run_checked(w, arrays=(k, v, qp, qd))
     assert not errs, "\n".join(errs[:20])
     assert (np.concatenate(paths) == 0).all()
+
+
+def test_recent_retrieval_ablation_against_oracle():
+    # Table 3's "recent-R retrieval": the R newest cache entries, rho_max over them
+    w = synth.scaled(synth.WORKLOADS["qwen7b_16k"], steps=24, recent=True, name="qwen7b_16k_recentR")
+    dr, errs, agg, paths = run_checked(w, check_steps=set(range(2, 25, 3)))
+    assert not errs, "\n".join(errs[:20])
+    topR = dr.ctx.retopk_get_diagnostics()["topR"]
+    assert (topR[:, 0] == w.C - 1).all() and (topR[:, 1] == w.C - 2).all()
 
 
 def test_fidelity_diagnostics_match_oracle():

@@ -44,6 +44,9 @@ MUTANTS = {
     "reuse_ignores_window": ("    total += L - lo;", "    total += 0; lo = L;"),
     "fidelity_mass_unnormalised": ("            const double p = exp(eS[a] - mS) / ZS, ph = exp(eh[b] - mh) / Zh;",
                                    "            const double p = exp(eS[a] - mS), ph = exp(eh[b] - mh) / Zh;"),
+    "recent_rho_max_over_all": ("        if (rho[n - 1 - r] > rmax)\n            rmax = rho[n - 1 - r];",
+                                "        (void)0;\n    }\n    for (int r = 0; r < n; ++r) {\n"
+                                "        if (rho[r] > rmax)\n            rmax = rho[r];"),
     "fidelity_recall_over_judged": ("    out[0] = nS > 0 ? (double)common / nS : 1.0;",
                                     "    out[0] = nh > 0 ? (double)common / nh : 1.0;"),
 }

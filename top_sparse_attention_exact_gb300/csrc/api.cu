@@ -110,6 +110,7 @@ size_t plan(const retopk_config &c, bool stateful, Work *w, char *base)
     x.R = c.R;
     x.T_r = c.T_r;
     x.tau = c.tau;
+    x.retrieval = c.retrieval;
     const int RKW = stateful ? c.R * c.K + c.W : 0;
     x.cand_stride = cand_stride_for(c.max_len, RKW);
     x.sc_stride = (c.max_len + 15) & ~15;
@@ -186,6 +187,8 @@ int check_cfg(const retopk_config *c)
     if ((long long)c->R * c->K + c->W > kMaxCand)
         return RETOPK_ERR_UNSUPPORTED;
     if (isnan(c->tau))
+        return RETOPK_ERR_INVALID;
+    if (c->retrieval != RETOPK_RETRIEVE_SIMILAR && c->retrieval != RETOPK_RETRIEVE_RECENT)
         return RETOPK_ERR_INVALID;
     return RETOPK_OK;
 }

@@ -32,6 +32,7 @@ enum { CNT_REUSE = 0, CNT_FALLBACK = 1, CNT_REFRESH = 2, CNT_SUM_M = 3, CNT_MAX_
 struct Work {
     int B, Hq, Hkv, G, max_len, K, C, W, R, T_r;
     float tau;
+    int retrieval;     // RETOPK_RETRIEVE_*
     int cand_stride;   // per-head capacity of cand_idx / cand_key
     int n_scan;        // scan CTAs per (b, h_kv)
     int sc_stride;     // row stride of `scores` (max_len rounded up to 16)

@@ -113,8 +113,20 @@ __global__ void __launch_bounds__(kDecideThreads) decide_kernel(DecideArgs a)
         sh.rho[c] = (sh.nq > 0.f && nc > 0.f) ? dq / (sqrtf(sh.nq) * sqrtf(nc)) : -INFINITY;
     }
     __syncthreads();
-    // Eq. (7): Top-R by (rho desc, older first)
-    for (int c = tid; c < count; c += kDecideThreads) {
+    // Eq. (7): Top-R by (rho desc, older first); or the R newest entries
+    if (w.retrieval == RETOPK_RETRIEVE_RECENT) {
+        const int nr = min(w.R, count);
+        for (int r = tid; r < nr; r += kDecideThreads)
+            sh.topr[r] = count - 1 - r;
+        __syncthreads();
+        if (tid == 0) {   // rho_max over the retrieved entries
+            float m = -INFINITY;
+            for (int r = 0; r < nr; ++r)
+                m = fmaxf(m, sh.rho[count - 1 - r]);
+            sh.nq = m;    // (|q|^2 is not needed any more)
+        }
+    }
+    for (int c = tid; c < count && w.retrieval != RETOPK_RETRIEVE_RECENT; c += kDecideThreads) {
         const float r = sh.rho[c];
         int rk = 0;
 #pragma unroll 8
@@ -125,7 +137,7 @@ __global__ void __launch_bounds__(kDecideThreads) decide_kernel(DecideArgs a)
         sh.topr[rk] = c;
     }
     __syncthreads();
-    const float rmax = count > 0 ? sh.rho[sh.topr[0]] : -INFINITY;
+    const float rmax = count == 0 ? -INFINITY : (w.retrieval == RETOPK_RETRIEVE_RECENT ? sh.nq : sh.rho[sh.topr[0]]);
     const bool refresh = (w.T_r > 0) && (t_dec % w.T_r == 0);   // Eq. (13), checked first
     const int p = refresh ? RETOPK_PATH_REFRESH : (!(rmax >= w.tau) ? RETOPK_PATH_FALLBACK : RETOPK_PATH_REUSE);
     if (tid == 0) {

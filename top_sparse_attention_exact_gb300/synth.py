@@ -71,6 +71,7 @@ class Workload:
     stay: float
     seeds: tuple = field(default_factory=tuple)
     d: int = 128
+    recent: bool = False   # the "recent-R retrieval" ablation instead of Eq. (7)
 
     @property
     def max_len(self) -> int:
