@@ -33,6 +33,9 @@ def test_every_declared_symbol_is_exported(lib):
 def test_config_validation_without_gpu(lib):
     ok = retopk.retopk_config(1, 28, 4, 128, 131584, 512, 32, 32, 4, 128, 0.85)
     assert lib.retopk_workspace_bytes(ctypes.byref(ok)) > 0
+    for good in (retopk.retopk_config(1, 28, 4, 128, 1 << 23, 512, 32, 32, 4, 128, 0.85),
+                 retopk.retopk_config(1, 28, 4, 128, 5095424, 4096, 8, 2048, 4, 128, 0.85)):
+        assert lib.retopk_workspace_bytes(ctypes.byref(good)) > 0
     bad = [
         retopk.retopk_config(1, 28, 4, 64, 1024, 512, 32, 32, 4, 128, 0.85),    # head_dim
         retopk.retopk_config(1, 28, 5, 128, 1024, 512, 32, 32, 4, 128, 0.85),   # Hq % Hkv
@@ -40,7 +43,11 @@ def test_config_validation_without_gpu(lib):
         retopk.retopk_config(1, 28, 4, 128, 1024, 0, 32, 32, 4, 128, 0.85),     # K
         retopk.retopk_config(1, 28, 4, 128, 1024, 512, 0, 32, 4, 128, 0.85),    # C
         retopk.retopk_config(1, 28, 4, 128, 1024, 512, 32, -1, 4, 128, 0.85),   # W
-        retopk.retopk_config(1, 28, 4, 128, 1 << 21, 512, 32, 32, 4, 128, 0.85),  # max_len
+        retopk.retopk_config(1, 28, 4, 128, (1 << 23) + 1, 512, 32, 32, 4, 128, 0.85),  # max_len
+        retopk.retopk_config(32, 28, 4, 128, 1 << 23, 512, 32, 32, 4, 128, 0.85),    # B*Hkv*max_len
+        retopk.retopk_config(1, 28, 4, 128, 1024, 4096, 8, 0, 5, 128, 0.85),         # R*K + W
+        # R*K + W = 18432: the bitmap slice of max_len / 8 positions no longer fits beside the lists
+        retopk.retopk_config(1, 28, 4, 128, 5095424 + 1, 4096, 8, 2048, 4, 128, 0.85),
         retopk.retopk_config(1, 28, 4, 128, 1024, 512, 32, 32, 4, 128, float("nan")),
         retopk.retopk_config(1, 28, 4, 128, 1024, 512, 32, 32, 4, 128, 0.85, 2),   # retrieval mode
     ]

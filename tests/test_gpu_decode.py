@@ -148,6 +148,30 @@ def _degenerate(tau, T_r, W, steps=12):
     return w
 
 
+def test_short_history_ranks_without_keys():
+    # L <= 64: the candidate bitmap's slices are 32 positions, so ranks 2..7 of
+    # each cluster own no position and contribute empty candidate lists
+    w = synth.scaled(synth.WORKLOADS["tiny_1h_2k"], L0=40, steps=24, K=16, C=8, W=8, R=2, tau=0.3,
+                     T_r=0, n_topics=4, run=8, name="tiny_short_history")
+    dr, errs, agg, paths = run_checked(w)
+    assert not errs, "\n".join(errs[:20])
+    assert (np.concatenate(paths) == 0).sum() >= 12
+
+
+def test_long_history_split_bitmap():
+    # 3M keys: each rank's bitmap slice covers ~393K positions and the
+    # retrieved supports spread over all of them
+    w = synth.scaled(synth.WORKLOADS["tiny_1h_2k"], L0=3_000_000, steps=8, K=512, tau=0.3, T_r=0,
+                     n_topics=16, run=256, name="tiny_3m")
+    dr, errs, agg, paths = run_checked(w)
+    assert not errs, "\n".join(errs[:20])
+    assert (np.concatenate(paths) == 0).sum() >= 4
+    diag = dr.ctx.retopk_get_diagnostics()
+    span = ((w.L0 + w.steps + 7) // 8 + 31) // 32 * 32
+    ranks = {int(i) // span for i in diag["support"][0] if i >= 0}
+    assert len(ranks) >= 4, ranks
+
+
 def test_tau_above_one_equals_exact_every_step():
     w = _degenerate(1.5, 0, 32)
     dr = DecodeRun(w)

@@ -141,6 +141,21 @@ def test_exact_qwen_shape_all_heads(name):
     assert not errs, "\n".join(errs[:20])
 
 
+def test_exact_longest_history():
+    # the largest supported history (2^20 - 1 keys): 8 segments of ~131K
+    # scores, each copied in several shared-memory slices
+    L = (1 << 20) - 1
+    q, k, v = gauss(9, 1, 2, 1, L)
+    idx, out = run_exact(q, k, v, [L], 512, max_len=1 << 20)
+    from parity import support_ok
+    for h in range(2):
+        sup, kth, ref = oracle.exact_one(q[0, h], k[0, 0], v[0, 0], L, 512)
+        ok, msg = support_ok(q[0, h], k[0, 0], idx[0, h], sup, kth)
+        assert ok, msg
+        ok, mx, rel = out_close(out[0, h], ref)
+        assert ok, (h, mx, rel)
+
+
 def test_exact_headline_128k_sampled_heads():
     w = synth.scaled(synth.WORKLOADS["qwen7b_128k"], steps=1)
     k, v, qp, qd = synth.generate(w)

@@ -14,6 +14,7 @@ namespace retopk {
 cudaError_t configure_scan();
 cudaError_t configure_select();
 cudaError_t configure_finish();
+size_t finish_smem_bytes_for(int max_len, int K, int RKW);
 cudaError_t configure_fidelity();
 }  // namespace retopk
 
@@ -170,7 +171,8 @@ int check_dims(int B, int Hq, int Hkv, int d, int max_len, int K)
         return RETOPK_ERR_INVALID;
     if (Hq % Hkv != 0)
         return RETOPK_ERR_INVALID;
-    if (d != kD || Hq / Hkv > kMaxGroup || max_len > kMaxLen || K > kMaxK || (long long)B * Hkv > kMaxSeqGroups)
+    if (d != kD || Hq / Hkv > kMaxGroup || max_len > kMaxLen || K > kMaxK || (long long)B * Hkv > kMaxSeqGroups ||
+        (long long)B * Hkv * max_len > kMaxRows)
         return RETOPK_ERR_UNSUPPORTED;
     return RETOPK_OK;
 }
@@ -185,6 +187,11 @@ int check_cfg(const retopk_config *c)
     if (c->C < 1 || c->C > kMaxC || c->R < 1 || c->R > c->C || c->W < 0 || c->T_r < 0)
         return RETOPK_ERR_INVALID;
     if ((long long)c->R * c->K + c->W > kMaxCand)
+        return RETOPK_ERR_UNSUPPORTED;
+    // the reuse path's bitmap slice and candidate lists share one CTA's shared
+    // memory; the query-support cache is addressed with 32-bit offsets
+    if (finish_smem_bytes_for(c->max_len, c->K, c->R * c->K + c->W) > kMaxDynSmem ||
+        (long long)c->batch * c->n_q_heads * c->C * c->K > INT32_MAX)
         return RETOPK_ERR_UNSUPPORTED;
     if (isnan(c->tau))
         return RETOPK_ERR_INVALID;

@@ -14,12 +14,14 @@ constexpr int kD = 128;             // head dimension (the only one supported)
 constexpr int kHistBits = 11;       // first-level radix digit of the exact scan
 constexpr int kHistBins = 1 << kHistBits;
 constexpr int kMaxGroup = 16;       // query heads per KV head
-constexpr int kMaxLen = 1 << 20;    // rows per sequence (candidate bitmap in smem)
+constexpr int kMaxLen = 1 << 23;    // rows per sequence
+constexpr long long kMaxRows = 1ll << 29;   // B * Hkv * max_len (the scan's TMA row coordinate is 32-bit)
 constexpr int kMaxK = 4096;
 constexpr int kMaxC = 256;
 constexpr int kExactCluster = 8;    // CTAs (candidate segments) per exact-path head
 constexpr int kMaxSeqGroups = 512;  // B * Hkv handled by one scan launch
-constexpr int kMaxCand = 20480;     // R*K + W (the candidate list lives in smem)
+constexpr int kMaxCand = 18432;     // R*K + W (the candidate lists live in smem)
+constexpr size_t kMaxDynSmem = 227 * 1024;   // dynamic shared memory of one CTA
 
 // Per-sequence control words.
 // (next slot, live entries, decode steps done, unused); `snap` holds the same

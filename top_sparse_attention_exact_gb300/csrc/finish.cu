@@ -14,10 +14,10 @@ namespace retopk {
 
 static_assert(kReuseThreads == kSelThreads && kReuseCluster == kExactCluster, "one launch shape for both paths");
 
-constexpr size_t kFinishMaxSmem = std::max(kReuseSharedBytes + ((size_t)(kMaxLen >> 5) + (size_t)kMaxCand) * 4,
-                                           kSelSharedBytes + kSelRegionBytes + (size_t)kLocCap * 8 +
-                                               (size_t)kMaxK * 8);
-static_assert(kFinishMaxSmem <= 227 * 1024, "largest configuration fits one CTA's shared memory");
+// the exact select fits for every K; the reuse path's size depends on max_len
+// and R*K + W together and is checked per configuration (finish_smem_bytes_for)
+static_assert(kSelSharedBytes + kSelRegionBytes + (size_t)kLocCap * 8 + (size_t)kMaxK * 8 <= kMaxDynSmem,
+              "the exact select fits one CTA's shared memory for every K");
 
 __global__ void __launch_bounds__(kSelThreads, 2) finish_kernel(SelArgs sa, ReuseArgs ra)
 {
@@ -44,9 +44,14 @@ __global__ void __launch_bounds__(kSelThreads, 2) finish_kernel(SelArgs sa, Reus
         exact_select_body(sa, fin_smem);
 }
 
+size_t finish_smem_bytes_for(int max_len, int K, int RKW)
+{
+    return std::max(sel_smem_bytes(K), reuse_smem_bytes(max_len, RKW));
+}
+
 static size_t finish_smem_bytes(const Work &w)
 {
-    return std::max(sel_smem_bytes(w.K), reuse_smem_bytes(w.max_len, w.R * w.K + w.W));
+    return finish_smem_bytes_for(w.max_len, w.K, w.R * w.K + w.W);
 }
 
 cudaError_t launch_finish(const Work &w, const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
@@ -72,7 +77,7 @@ cudaError_t launch_finish(const Work &w, const uint16_t *q, const uint16_t *k_ca
 cudaError_t configure_finish()
 {
     cudaError_t e =
-        cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFinishMaxSmem);
+        cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxDynSmem);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(finish_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared);

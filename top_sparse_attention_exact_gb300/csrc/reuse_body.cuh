@@ -4,10 +4,14 @@
 // Implementation: candidate union and dedup, indexed rerank, Top-K, indexed
 // softmax-value aggregation and cache update), after the path decision.
 //
-// Every CTA of the cluster builds the candidate set A_t (Eqs. (8)-(9): window
-// U the retrieved supports) through a shared-memory bitmap of L bits,
-// emitted in ascending order, so that the cluster agrees on A_t without
-// communication.  The work that touches HBM is split across the cluster:
+// The candidate set A_t (Eqs. (8)-(9): window U the retrieved supports) is
+// built through a bitmap over the key positions split across the cluster:
+// rank r owns the positions [r*S, (r+1)*S) (S = L/kReuseCluster rounded up to
+// 32), sets the bits of the window and support entries in that range in its
+// own shared memory, and lists its candidates in ascending order.  After one
+// cluster barrier every rank concatenates the eight lists in rank order
+// (distributed shared memory reads), so the cluster agrees on A_t, ascending.
+// The work that touches HBM is split across the cluster:
 //   Eq. (10) each CTA scores 1/kReuseCluster of the candidate keys (K rows
 //            gathered straight from the cache) and pushes the scores into
 //            every peer's shared memory (distributed shared memory);
@@ -51,23 +55,46 @@ struct ReuseShared {
     int pre[kMaxC + 1];    // prefix of the retrieved supports' lengths
     int sup_off[kMaxC];    // cache offset of each retrieved support
     int wcount[kReuseWarps];
+    int ncand;             // this rank's candidates (read by the peers)
+    int cpre[kReuseCluster + 1];   // prefix of the ranks' candidate counts
     uint32_t kmax;
     SelectShared sel;
-    alignas(16) float red[kReuseWarps][kD];          // written with 16-byte stores
+};
+// value-phase scratch (after the scores are exchanged)
+struct ReuseTail {
+    float red[kReuseWarps][kD];          // written with 16-byte stores
     float zw[kReuseWarps];
-    alignas(16) float part_o[kReuseCluster][kD];     // rank 0 receives every rank's partial
+    alignas(16) float part_o[kReuseCluster][kD];   // rank 0 receives every rank's partial
     float part_z[kReuseCluster];
 };
-static_assert(offsetof(ReuseShared, red) % 16 == 0, "16-byte stores into red");
-static_assert(offsetof(ReuseShared, part_o) % 16 == 0, "partials aligned");
-// the per-CTA state leads the dynamic shared memory; then the bitmap / score
-// region and the candidate list
+static_assert(offsetof(ReuseTail, part_o) % 16 == 0, "partials aligned");
+constexpr int kReuseTailWords = (int)((sizeof(ReuseTail) + 15) / 16 * 4);
+
+// Dynamic shared memory of the reuse path, in 4-byte words after ReuseShared:
+//   [0, A)        the rank's bitmap slice; then the M_t scores (keys)
+//   [A, A + Bw)   the rank's list of candidates; then the ReuseTail
+//   [A + Bw, +RKW) A_t, then S_t (cand)
+// with A = max(S/32, RKW) rounded up to 4 and Bw = max(RKW, kReuseTailWords).
 constexpr size_t kReuseSharedBytes = (sizeof(ReuseShared) + 127) & ~size_t(127);
+
+// positions per rank of the split bitmap: L / kReuseCluster rounded up to 32
+__host__ __device__ __forceinline__ int reuse_span(int L)
+{
+    return (((L + kReuseCluster - 1) / kReuseCluster) + 31) & ~31;
+}
+__host__ __device__ __forceinline__ int reuse_words_a(int max_len, int RKW)
+{
+    const int s = reuse_span(max_len) >> 5;
+    return ((s > RKW ? s : RKW) + 3) & ~3;
+}
+__host__ __device__ __forceinline__ int reuse_words_b(int RKW)
+{
+    return RKW > kReuseTailWords ? RKW : kReuseTailWords;
+}
 
 inline size_t reuse_smem_bytes(int max_len, int RKW)
 {
-    const size_t region = (size_t)std::max((max_len + 31) >> 5, RKW);
-    return kReuseSharedBytes + (region + (size_t)RKW) * 4;
+    return kReuseSharedBytes + ((size_t)reuse_words_a(max_len, RKW) + reuse_words_b(RKW) + (size_t)RKW) * 4;
 }
 
 // Eqs. (8)-(12) and the cache insertion for one reuse head per cluster of
@@ -85,10 +112,12 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
     if (w.path[bh] != RETOPK_PATH_REUSE)
         return;                                   // uniform over the cluster
     const int RKW = w.R * w.K + w.W;
-    uint32_t *region = rsm;                                           // bitmap, then the scores
-    const int region_words = max((w.max_len + 31) >> 5, RKW);
-    int32_t *cand = reinterpret_cast<int32_t *>(rsm + region_words);  // A_t, then S_t
+    const int wa = reuse_words_a(w.max_len, RKW), wb = reuse_words_b(RKW);
+    uint32_t *region = rsm;                                           // bitmap slice, then the scores
     uint32_t *keys = region;
+    int32_t *loc = reinterpret_cast<int32_t *>(rsm + wa);             // this rank's candidates
+    ReuseTail &tl = *reinterpret_cast<ReuseTail *>(rsm + wa);         // (after the score exchange)
+    int32_t *cand = reinterpret_cast<int32_t *>(rsm + wa + wb);       // A_t, then S_t
 
     // ---- the decision's outputs: retrieved entries and their supports --------
     const int L = seq_len(a.seqlens, b, 0, w.max_len);
@@ -117,24 +146,27 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
         if (tid == 0)
             sh.pre[nr] = tot;
     }
-    const int nwords = (L + 31) >> 5;
+    // this rank's positions [r_lo, r_hi) (r_lo a multiple of 32)
+    const int r_lo = min(L, rank * reuse_span(L)), r_hi = min(L, r_lo + reuse_span(L));
+    const int nwords = (r_hi - r_lo + 31) >> 5;
     for (int i = tid; i < nwords; i += kReuseThreads)
         region[i] = 0u;
     __syncthreads();
 
-    // ---- Eqs. (8)-(9): candidate bitmap -------------------------------------
+    // ---- Eqs. (8)-(9): candidate bitmap (this rank's slice) -----------------
     // recent window [lo, L): one thread per bitmap word
-    const int lo = max(0, L - w.W);
-    if (lo < L) {
-        for (int wd = (lo >> 5) + tid; wd <= ((L - 1) >> 5); wd += kReuseThreads) {
-            const int a0 = max(lo, wd << 5) - (wd << 5), a1 = min(L, (wd << 5) + 32) - (wd << 5);
+    const int lo = max(r_lo, L - w.W);
+    if (lo < r_hi) {
+        for (int wd = ((lo - r_lo) >> 5) + tid; wd <= ((r_hi - 1 - r_lo) >> 5); wd += kReuseThreads) {
+            const int p0 = r_lo + (wd << 5);
+            const int a0 = max(lo, p0) - p0, a1 = min(r_hi, p0 + 32) - p0;
             const uint32_t msk = (a1 - a0 == 32) ? 0xffffffffu : (((1u << (a1 - a0)) - 1u) << a0);
             atomicOr(&region[wd], msk);
         }
     }
     // thread t walks a contiguous run of the concatenated (ascending) support
     // lists, so neighbouring indices share a bitmap word: OR them in a register
-    // and issue one shared atomic per word change
+    // and issue one shared atomic per word change (entries of this rank only)
     const int T = sh.pre[nr];
     {
         const int per_t = (T + kReuseThreads - 1) / kReuseThreads;
@@ -162,8 +194,8 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
                 if (e0 + u >= e_end)
                     break;
                 const int i = id[u];
-                if (i >= 0 && i < L) {
-                    const uint32_t wd = (uint32_t)i >> 5, bit = 1u << (i & 31);
+                if (i >= r_lo && i < r_hi) {
+                    const uint32_t wd = (uint32_t)(i - r_lo) >> 5, bit = 1u << (i & 31);
                     if (wd != cur_w) {
                         if (cur_m)
                             atomicOr(&region[cur_w], cur_m);
@@ -171,7 +203,7 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
                         cur_m = 0u;
                     }
                     cur_m |= bit;
-                } else if (rank == 0) {
+                } else if ((i < 0 || i >= L) && rank == 0) {
                     atomicOr(w.status, RETOPK_STATUS_BAD_INDEX);
                 }
             }
@@ -180,9 +212,10 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
             atomicOr(&region[cur_w], cur_m);
     }
     __syncthreads();
-    // ascending emission.  Warp v owns a contiguous range of bitmap words and
-    // walks it 32 words at a time, lane l taking word l of each chunk, so that
-    // dense stretches (a retrieved topic run) are shared by all lanes.
+    // ascending emission of this rank's list.  Warp v owns a contiguous range
+    // of bitmap words and walks it 32 words at a time, lane l taking word l of
+    // each chunk, so that dense stretches (a retrieved topic run) are shared
+    // by all lanes.
     const int chunks = (nwords + kReuseWarps * 32 - 1) / (kReuseWarps * 32);   // per warp
     const int wbeg = warp * chunks * 32;
     int mine = 0;
@@ -194,11 +227,13 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
     if (lane == 0)
         sh.wcount[warp] = mine;
     __syncthreads();
-    int pos = 0, M = 0;
+    int pos = 0, Mr = 0;
     for (int v = 0; v < kReuseWarps; ++v) {
         pos += (v < warp) ? sh.wcount[v] : 0;
-        M += sh.wcount[v];
+        Mr += sh.wcount[v];
     }
+    if (tid == 0)
+        sh.ncand = Mr;
     const unsigned lt = (1u << lane) - 1u;
     for (int k = 0; k < chunks; ++k) {
         const int i = wbeg + k * 32 + lane;
@@ -223,18 +258,52 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
             const uint32_t wb = __shfl_sync(0xffffffffu, bits, src);
             const int base = __shfl_sync(0xffffffffu, excl, src);
             if ((wb >> lane) & 1u)
-                cand[base + __popc(wb & lt)] = ((wbeg + k * 32 + src) << 5) + lane;
+                loc[base + __popc(wb & lt)] = r_lo + ((wbeg + k * 32 + src) << 5) + lane;
         }
         pos += __shfl_sync(0xffffffffu, incl, 31);
     }
+    // every rank's list and count are complete, and every bitmap is dead (the
+    // peers' scores may now land in the region that held it)
+    cluster.sync();
+    if (tid < kReuseCluster)
+        sh.cpre[tid + 1] = *cluster.map_shared_rank(&sh.ncand, tid);
     __syncthreads();
-    if (rank == 0) {
-        int32_t *ci = w.cand_idx + (size_t)bh * w.cand_stride;
-        for (int j = tid; j < M; j += kReuseThreads)
-            ci[j] = cand[j];
-        if (tid == 0)
+    if (tid == 0) {
+        sh.cpre[0] = 0;
+        for (int r = 0; r < kReuseCluster; ++r)
+            sh.cpre[r + 1] += sh.cpre[r];
+    }
+    __syncthreads();
+    const int M = sh.cpre[kReuseCluster];
+    {   // A_t = the ranks' lists in rank order; four peer loads in flight
+        for (int j0 = tid; j0 < M; j0 += 4 * kReuseThreads) {
+            int32_t v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u * kReuseThreads;
+                v[u] = 0;
+                if (j < M) {
+                    int r = 0;
+#pragma unroll
+                    for (int q = 1; q < kReuseCluster; ++q)
+                        r += j >= sh.cpre[q];
+                    v[u] = cluster.map_shared_rank(loc, r)[j - sh.cpre[r]];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u * kReuseThreads;
+                if (j < M)
+                    cand[j] = v[u];
+            }
+        }
+        int32_t *ci = w.cand_idx + (size_t)bh * w.cand_stride + sh.cpre[rank];
+        for (int j = tid; j < Mr; j += kReuseThreads)
+            ci[j] = loc[j];
+        if (rank == 0 && tid == 0)
             w.M[bh] = M;
     }
+    __syncthreads();
 
     // ---- Eq. (10): this rank's slice of the candidate scores -----------------
     const int per = (M + kReuseCluster - 1) / kReuseCluster;
@@ -269,10 +338,8 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
             }
         }
     }
-    // every CTA of the cluster is past its bitmap before any score is pushed
-    // into the (shared) region that held it
-    cluster.sync();
-    // push the slice into every peer
+    __syncthreads();   // the slice's scores are written
+    // push the slice into every peer (each is past its bitmap: cluster barrier above)
     for (int e = tid; e < (ce - cs) * (kReuseCluster - 1); e += kReuseThreads) {
         const int p = e / (ce - cs), j = cs + e % (ce - cs);
         const int peer = p < rank ? p : p + 1;
@@ -326,23 +393,23 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
     float zsum = 0.f;
     const uint16_t *vb = a.v + ((size_t)(b * w.Hkv + hk) * w.max_len) * kD;
     value_partial<8>(vb, sup_i, sup_k, vs + warp, ve, kReuseWarps, m, acc, zsum);
-    *reinterpret_cast<float4 *>(&sh.red[warp][lane * 4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4 *>(&tl.red[warp][lane * 4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     if (lane == 0)
-        sh.zw[warp] = zsum;
+        tl.zw[warp] = zsum;
     __syncthreads();
     if (tid < kD) {
         float o = 0.f;
 #pragma unroll
         for (int ww = 0; ww < kReuseWarps; ++ww)
-            o += sh.red[ww][tid];
-        cluster.map_shared_rank(&sh.part_o[0][0], 0)[rank * kD + tid] = o;
+            o += tl.red[ww][tid];
+        cluster.map_shared_rank(&tl.part_o[0][0], 0)[rank * kD + tid] = o;
     }
     if (tid == kD) {
         float z = 0.f;
 #pragma unroll
         for (int ww = 0; ww < kReuseWarps; ++ww)
-            z += sh.zw[ww];
-        cluster.map_shared_rank(&sh.part_z[0], 0)[rank] = z;
+            z += tl.zw[ww];
+        cluster.map_shared_rank(&tl.part_z[0], 0)[rank] = z;
     }
     cluster.sync();
     if (rank != 0)
@@ -353,8 +420,8 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
         float o = 0.f, Z = 0.f;
 #pragma unroll
         for (int r = 0; r < kReuseCluster; ++r) {
-            o += sh.part_o[r][tid];
-            Z += sh.part_z[r];
+            o += tl.part_o[r][tid];
+            Z += tl.part_z[r];
         }
         o = (n > 0) ? o / Z : 0.f;
         a.out[(size_t)bh * kD + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(o));

@@ -92,6 +92,11 @@ WORKLOADS = {
                            64, 256, 0.95, (3,)),
     "qwen7b_128k": Workload("qwen7b_128k", 1, 28, 4, 131072, 512, 512, 32, 32, 4, 0.85, 128,
                             64, 256, 0.95, (4,)),
+    # the long-context scaling lengths (1M and 5M keys, 2^20 and 5 * 2^20)
+    "qwen7b_1m": Workload("qwen7b_1m", 1, 28, 4, 1048576 - 256, 256, 512, 32, 32, 4, 0.85, 128,
+                          64, 256, 0.95, (5,)),
+    "qwen7b_5m": Workload("qwen7b_5m", 1, 28, 4, 5242880 - 256, 256, 512, 32, 32, 4, 0.85, 128,
+                          64, 256, 0.95, (6,)),
 }
 
 
