@@ -158,6 +158,25 @@ int retopk_decode_step_kv(retopk_ctx *ctx, const retopk_bf16 *k_new, const retop
                           const retopk_bf16 *q, retopk_bf16 *k_cache, retopk_bf16 *v_cache,
                           int32_t *d_seqlens, retopk_bf16 *out, void *stream);
 
+/* retopk_decode_step_kv with the token's inputs and the output in HOST memory
+ * (pageable or pinned): k_new / v_new [B, Hkv, d], q [B, Hq, d], out
+ * [B, Hq, d], all bf16 on the host; k_cache, v_cache, d_seqlens stay on the
+ * device.  Synchronous: returns once `out` holds the step's output.  The
+ * inputs are copied into library-owned pinned, device-mapped memory; the
+ * three kernels of retopk_decode_step_kv are replayed as a CUDA graph on
+ * `stream` (captured on the first call and again whenever k_cache, v_cache or
+ * d_seqlens change), the path-decision kernel reading the token's q, k_new,
+ * v_new across the host link (and copying q to device memory for the later
+ * kernels) and the back end writing the output rows into the mapped buffer,
+ * which is then copied to `out`.  The first call allocates the staging
+ * (pinned: 2 B Hq d * 2 + 2 B Hkv d * 2 bytes; device: 2 B Hq d bytes),
+ * freed by retopk_destroy.  Not to be called from several threads on one
+ * context, nor during stream capture.  Same results as retopk_decode_step_kv
+ * on the same inputs. */
+int retopk_decode_step_host(retopk_ctx *ctx, const retopk_bf16 *k_new, const retopk_bf16 *v_new,
+                            const retopk_bf16 *q, retopk_bf16 *k_cache, retopk_bf16 *v_cache,
+                            int32_t *d_seqlens, retopk_bf16 *out, void *stream);
+
 /* Per-step diagnostics of the last decode step, copied to HOST buffers
  * (synchronises `stream`).  Any pointer may be NULL.
  *   path     [B*Hq] int32   RETOPK_PATH_*

@@ -172,6 +172,35 @@ def test_long_history_split_bitmap():
     assert len(ranks) >= 4, ranks
 
 
+def test_host_buffer_step_matches_device_step():
+    # retopk_decode_step_host (host inputs/outputs, graph replay) against
+    # retopk_decode_step_kv on a second context with the same inputs: identical
+    # outputs and supports every step; then a second pair of caches (the graph
+    # is captured again for the new binding)
+    w = synth.scaled(synth.WORKLOADS["qwen7b_16k"], L0=4096, steps=20, T_r=8, name="host_api")
+    arrays = synth.generate(w)
+    dev_run, host_run = DecodeRun(w, arrays=arrays), DecodeRun(w, arrays=arrays)
+    qh = torch.from_numpy(np.ascontiguousarray(arrays[3]).view(np.int16))
+    kh = torch.from_numpy(np.ascontiguousarray(arrays[0][:, :, w.L0:].transpose(2, 0, 1, 3)).view(np.int16))
+    vh = torch.from_numpy(np.ascontiguousarray(arrays[1][:, :, w.L0:].transpose(2, 0, 1, 3)).view(np.int16))
+    out_h = torch.zeros((w.B, w.Hq, w.d), dtype=torch.int16).pin_memory()
+    for t in range(w.steps):
+        if t == 12:   # move the host run's caches to new allocations
+            host_run.k_cache, host_run.v_cache = host_run.k_cache.clone(), host_run.v_cache.clone()
+            host_run.seqlens = host_run.seqlens.clone()
+        dev_run.step(t)
+        src_q = qh[t] if t % 2 else qh[t].clone().pin_memory()   # pageable and pinned inputs
+        host_run.ctx.retopk_decode_step_host(kh[t], vh[t], src_q, host_run.k_cache, host_run.v_cache,
+                                             host_run.seqlens, out_h)
+        torch.cuda.synchronize()
+        assert torch.equal(out_h, dev_run.out.cpu()), t
+        da, db = dev_run.ctx.retopk_get_diagnostics(), host_run.ctx.retopk_get_diagnostics()
+        for key in ("path", "support", "sup_len", "M"):
+            assert np.array_equal(da[key], db[key]), (t, key)
+    assert torch.equal(host_run.k_cache, dev_run.k_cache) and torch.equal(host_run.seqlens, dev_run.seqlens)
+    assert host_run.ctx.retopk_get_status() == 0
+
+
 def test_tau_above_one_equals_exact_every_step():
     w = _degenerate(1.5, 0, 32)
     dr = DecodeRun(w)

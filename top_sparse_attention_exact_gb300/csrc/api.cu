@@ -20,12 +20,27 @@ cudaError_t configure_fidelity();
 
 using namespace retopk;
 
+// State of retopk_decode_step_host: pinned and device staging for the step's
+// inputs and output, and the step captured as a CUDA graph for one binding of
+// the caches and lengths (captured again when the binding changes).
+struct HostStep {
+    unsigned char *pin;     // pinned, mapped: q | k_new | v_new | out
+    unsigned char *pin_d;   // its device address
+    unsigned char *dev;     // device copy of q
+    size_t o_k, o_v, o_out, bytes;
+    cudaStream_t cap;       // capture stream
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+    const void *k_cache, *v_cache, *seqlens;
+};
+
 struct retopk_ctx {
     retopk_config cfg;
     Work w;
     void *ws;
     size_t ws_bytes;
     int device;
+    HostStep hs;
 };
 
 namespace {
@@ -338,10 +353,30 @@ int retopk_create(const retopk_config *cfg, void *d_workspace, size_t bytes, ret
     return RETOPK_OK;
 }
 
+namespace {
+
+void release_host_step(HostStep &h)
+{
+    if (h.exec)
+        cudaGraphExecDestroy(h.exec);
+    if (h.graph)
+        cudaGraphDestroy(h.graph);
+    if (h.cap)
+        cudaStreamDestroy(h.cap);
+    if (h.dev)
+        cudaFree(h.dev);
+    if (h.pin)
+        cudaFreeHost(h.pin);
+    memset(&h, 0, sizeof h);
+}
+
+}  // namespace
+
 int retopk_destroy(retopk_ctx *ctx)
 {
     if (!ctx)
         return RETOPK_ERR_INVALID;
+    release_host_step(ctx->hs);
     free(ctx);
     return RETOPK_OK;
 }
@@ -396,22 +431,25 @@ int retopk_append_kv(retopk_ctx *ctx, const retopk_bf16 *k_new, const retopk_bf1
 
 namespace {
 
-// decide (with the append when k_new != null) -> scan -> finish
+// decide (with the append when k_new != null) -> scan -> finish.  With q_dev
+// != null the decision reads q where it is (e.g. mapped host memory) and
+// copies it to q_dev, from which the scan and the finish read it.
 int decode_step(retopk_ctx *ctx, const retopk_bf16 *k_new, const retopk_bf16 *v_new, const retopk_bf16 *q,
                 retopk_bf16 *k_cache, retopk_bf16 *v_cache, int32_t *d_seqlens, retopk_bf16 *out,
-                cudaStream_t st)
+                cudaStream_t st, retopk_bf16 *q_dev = nullptr)
 {
     const Work &w = ctx->w;
-    QSrc qs{q, (long long)w.Hq * kD, kD};
+    const retopk_bf16 *qk = q_dev ? q_dev : q;   // q as the scan and the finish read it
+    QSrc qs{qk, (long long)w.Hq * kD, kD};
     int e;
     if ((e = cuda_rc(timed(RETOPK_PROF_DECIDE, st, [&] {
-             return launch_decide(w, q, k_new, v_new, k_cache, v_cache, d_seqlens, st);
+             return launch_decide(w, q, q_dev, k_new, v_new, k_cache, v_cache, d_seqlens, st);
          }))))
         return e;
     if ((e = run_scan(w, qs, k_cache, d_seqlens, 0, st)))
         return e;
     return cuda_rc(timed(RETOPK_PROF_FINISH, st,
-                         [&] { return launch_finish(w, q, k_cache, v_cache, d_seqlens, out, st); }));
+                         [&] { return launch_finish(w, qk, k_cache, v_cache, d_seqlens, out, st); }));
 }
 
 }  // namespace
@@ -442,6 +480,87 @@ int retopk_decode_step_kv(retopk_ctx *ctx, const retopk_bf16 *k_new, const retop
         !aligned16(out))
         return RETOPK_ERR_ALIGN;
     return decode_step(ctx, k_new, v_new, q, k_cache, v_cache, d_seqlens, out, (cudaStream_t)stream);
+}
+
+int retopk_decode_step_host(retopk_ctx *ctx, const retopk_bf16 *k_new, const retopk_bf16 *v_new,
+                            const retopk_bf16 *q, retopk_bf16 *k_cache, retopk_bf16 *v_cache,
+                            int32_t *d_seqlens, retopk_bf16 *out, void *stream)
+{
+    if (!ctx || !k_new || !v_new || !q || !k_cache || !v_cache || !d_seqlens || !out)
+        return RETOPK_ERR_INVALID;
+    if (!aligned16(k_cache) || !aligned16(v_cache))
+        return RETOPK_ERR_ALIGN;
+    HostStep &h = ctx->hs;
+    const Work &w = ctx->w;
+    const size_t nq = (size_t)w.B * w.Hq * kD * 2, nkv = (size_t)w.B * w.Hkv * kD * 2;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t ce = cudaSuccess;
+    if (!h.pin) {
+        auto up = [](size_t x) { return (x + kAlign - 1) / kAlign * kAlign; };
+        h.o_k = up(nq);
+        h.o_v = h.o_k + up(nkv);
+        h.o_out = h.o_v + up(nkv);
+        h.bytes = h.o_out + up(nq);
+        ce = cudaHostAlloc((void **)&h.pin, h.bytes, cudaHostAllocMapped);
+        if (ce == cudaSuccess)
+            ce = cudaHostGetDevicePointer((void **)&h.pin_d, h.pin, 0);
+        if (ce == cudaSuccess)
+            ce = cudaMalloc((void **)&h.dev, nq);
+        if (ce == cudaSuccess)
+            ce = cudaStreamCreateWithFlags(&h.cap, cudaStreamNonBlocking);
+        if (ce != cudaSuccess) {
+            release_host_step(h);
+            return cuda_rc(ce);
+        }
+    }
+    if (!h.exec || h.k_cache != k_cache || h.v_cache != v_cache || h.seqlens != d_seqlens) {
+        // capture the decode step on the mapped staging: the decision reads the
+        // token's q, k_new, v_new across the host link (copying q to device
+        // memory for the later kernels) and the finish writes the output there
+        if (h.exec) {
+            cudaGraphExecDestroy(h.exec);
+            h.exec = nullptr;
+        }
+        if (h.graph) {
+            cudaGraphDestroy(h.graph);
+            h.graph = nullptr;
+        }
+        ce = cudaStreamBeginCapture(h.cap, cudaStreamCaptureModeThreadLocal);
+        if (ce != cudaSuccess)
+            return cuda_rc(ce);
+        const int e = decode_step(ctx, (const retopk_bf16 *)(h.pin_d + h.o_k), (const retopk_bf16 *)(h.pin_d + h.o_v),
+                                  (const retopk_bf16 *)h.pin_d, k_cache, v_cache, d_seqlens,
+                                  (retopk_bf16 *)(h.pin_d + h.o_out), h.cap, (retopk_bf16 *)h.dev);
+        cudaGraph_t g = nullptr;
+        ce = cudaStreamEndCapture(h.cap, &g);
+        if (e) {
+            if (g)
+                cudaGraphDestroy(g);
+            return e;
+        }
+        if (ce == cudaSuccess)
+            ce = cudaGraphInstantiate(&h.exec, g, 0);
+        if (ce != cudaSuccess) {
+            if (g)
+                cudaGraphDestroy(g);
+            h.exec = nullptr;
+            return cuda_rc(ce);
+        }
+        h.graph = g;
+        h.k_cache = k_cache;
+        h.v_cache = v_cache;
+        h.seqlens = d_seqlens;
+    }
+    memcpy(h.pin, q, nq);
+    memcpy(h.pin + h.o_k, k_new, nkv);
+    memcpy(h.pin + h.o_v, v_new, nkv);
+    ce = cudaGraphLaunch(h.exec, st);
+    if (ce == cudaSuccess)
+        ce = cudaStreamSynchronize(st);
+    if (ce != cudaSuccess)
+        return cuda_rc(ce);
+    memcpy(out, h.pin + h.o_out, nq);
+    return RETOPK_OK;
 }
 
 int retopk_fidelity(retopk_ctx *ctx, const retopk_bf16 *q, const retopk_bf16 *k_cache, const int32_t *exact_idx,

@@ -18,6 +18,9 @@ static_assert(kMaxC <= kDecideThreads, "one cache entry per thread");
 struct DecideArgs {
     Work w;
     const uint16_t *q;
+    // when not null, each CTA copies its head's q row here (the step's later
+    // kernels read q from this device copy; q itself may be host memory)
+    uint16_t *q_copy;
     // the token's K/V rows when the append is fused into this launch (else null)
     const uint16_t *k_new, *v_new;
     uint16_t *k_cache, *v_cache;
@@ -73,6 +76,9 @@ __global__ void __launch_bounds__(kDecideThreads) decide_kernel(DecideArgs a)
     }
     if (tid < kD)
         sh.qf[tid] = __uint_as_float(((uint32_t)a.q[(size_t)bh * kD + tid]) << 16);
+    if (a.q_copy && tid < kD / 8)
+        reinterpret_cast<uint4 *>(a.q_copy + (size_t)bh * kD)[tid] =
+            reinterpret_cast<const uint4 *>(a.q + (size_t)bh * kD)[tid];
     const uint2 qraw = *reinterpret_cast<const uint2 *>(a.q + (size_t)bh * kD + lane * 4);
     const float q0 = bf16lo(qraw.x), q1 = bf16hi(qraw.x), q2 = bf16lo(qraw.y), q3 = bf16hi(qraw.y);
     for (int s0 = warp * 4; s0 < w.C; s0 += (kDecideThreads / 32) * 4) {
@@ -153,10 +159,11 @@ __global__ void __launch_bounds__(kDecideThreads) decide_kernel(DecideArgs a)
     }
 }
 
-cudaError_t launch_decide(const Work &w, const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
-                          uint16_t *k_cache, uint16_t *v_cache, int32_t *seqlens, cudaStream_t st)
+cudaError_t launch_decide(const Work &w, const uint16_t *q, uint16_t *q_copy, const uint16_t *k_new,
+                          const uint16_t *v_new, uint16_t *k_cache, uint16_t *v_cache, int32_t *seqlens,
+                          cudaStream_t st)
 {
-    const DecideArgs a{w, q, k_new, v_new, k_cache, v_cache, seqlens};
+    const DecideArgs a{w, q, q_copy, k_new, v_new, k_cache, v_cache, seqlens};
     return launch_pdl(decide_kernel, dim3(w.B * w.Hq), dim3(kDecideThreads), 0, st, 1, a);
 }
 

@@ -27,7 +27,8 @@ EXPORTED = ("retopk_workspace_bytes", "retopk_create", "retopk_destroy", "retopk
             "retopk_import_state", "retopk_get_status", "retopk_strerror", "retopk_cuda_error_string",
             "exact_topk_workspace_bytes", "exact_topk_attention_step",
             "retopk_profile_enable", "retopk_profile_read", "retopk_profile_reset",
-            "retopk_selftest_wait", "exact_topk_attention_step_noalloc", "retopk_fidelity")
+            "retopk_selftest_wait", "exact_topk_attention_step_noalloc", "retopk_fidelity",
+            "retopk_decode_step_host")
 
 PROF_KERNELS = ("append", "finish", "scan", "select", "clear", "decide")
 
@@ -57,6 +58,7 @@ def _declare(lib):
     lib.retopk_append_kv.argtypes = [_P, _P, _P, _P, _P, _P, _P]
     lib.retopk_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P]
     lib.retopk_decode_step_kv.argtypes = [_P] * 9
+    lib.retopk_decode_step_host.argtypes = [_P] * 9
     lib.retopk_fidelity.argtypes = [_P] * 8
     lib.retopk_get_diagnostics.argtypes = [_P] + [_P] * 8 + [_P]
     lib.retopk_get_counters.argtypes = [_P, _P, _P]
@@ -120,8 +122,20 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _hptr(t: torch.Tensor, numel: int):
+    """Host (CPU) tensor of exactly `numel` elements, contiguous."""
+    if t.is_cuda:
+        raise RetopkError("expected a host (CPU) tensor")
+    if not t.is_contiguous() or t.numel() != numel:
+        raise RetopkError(f"expected a contiguous host tensor of {numel} elements, got {tuple(t.shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+_BF16_TYPES = (torch.bfloat16, torch.int16, torch.uint16)
+
+
 def _bf16(t: torch.Tensor) -> torch.Tensor:
-    if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+    if t.dtype not in _BF16_TYPES:
         raise RetopkError(f"bf16 tensor expected, got {t.dtype}")
     return t
 
@@ -236,6 +250,27 @@ class ReTopK:
         _check(load().retopk_decode_step_kv(self.handle, _ptr(_bf16(k_new)), _ptr(_bf16(v_new)), _ptr(_bf16(q)),
                                             _ptr(_bf16(k_cache)), _ptr(_bf16(v_cache)), _ptr(_i32(seqlens)),
                                             _ptr(_bf16(out)), _stream(stream)), "retopk_decode_step_kv")
+        return out
+
+    def retopk_decode_step_host(self, k_new, v_new, q, k_cache, v_cache, seqlens, out, stream=None):
+        """retopk_decode_step_kv with k_new / v_new / q / out in host memory
+        (CPU tensors, pinned or not); returns once `out` holds the output.
+        The device tensors and the stream are validated once per binding; each
+        call checks the four host tensors and passes their addresses."""
+        s = stream if stream is not None else torch.cuda.current_stream()
+        key = (k_cache.data_ptr(), v_cache.data_ptr(), seqlens.data_ptr(), s.cuda_stream)
+        if getattr(self, "_host_key", None) != key:
+            _ptr(_bf16(k_cache)), _ptr(_bf16(v_cache)), _ptr(_i32(seqlens))
+            self._host_key = key
+            self._host_fn = load().retopk_decode_step_host
+        nq, nkv = self.B * self.Hq * 128, self.B * self.Hkv * 128
+        for t, n in ((k_new, nkv), (v_new, nkv), (q, nq), (out, nq)):
+            if t.is_cuda or t.dtype not in _BF16_TYPES or t.numel() != n or not t.is_contiguous():
+                _hptr(_bf16(t), n)   # raises with the reason
+        rc = self._host_fn(self.handle, k_new.data_ptr(), v_new.data_ptr(), q.data_ptr(), key[0], key[1], key[2],
+                           out.data_ptr(), key[3])
+        if rc:
+            _check(rc, "retopk_decode_step_host")
         return out
 
     def retopk_fidelity(self, q, k_cache, exact_idx, out_exact, out, stream=None):
