@@ -158,6 +158,16 @@ def test_short_history_ranks_without_keys():
     assert (np.concatenate(paths) == 0).sum() >= 12
 
 
+def test_largest_max_len_short_history():
+    # max_len = 2^23: the reuse path's bitmap slice is 2^20 positions (128 KB)
+    # per CTA, the back end runs one CTA per SM; the history itself is short
+    w = synth.scaled(synth.WORKLOADS["tiny_1h_2k"], L0=4096, steps=16, Hq=2, K=128, tau=0.5, T_r=8,
+                     name="tiny_maxlen_2p23")
+    dr, errs, agg, paths = run_checked(w, max_len=1 << 23)
+    assert not errs, "\n".join(errs[:20])
+    assert (np.concatenate(paths) == 0).sum() >= 4
+
+
 def test_long_history_split_bitmap():
     # 3M keys: each rank's bitmap slice covers ~393K positions and the
     # retrieved supports spread over all of them

@@ -141,12 +141,14 @@ def test_exact_qwen_shape_all_heads(name):
     assert not errs, "\n".join(errs[:20])
 
 
-def test_exact_longest_history():
-    # the largest supported history (2^20 - 1 keys): 8 segments of ~131K
-    # scores, each copied in several shared-memory slices
-    L = (1 << 20) - 1
+@pytest.mark.parametrize("L,max_len", [((1 << 20) - 1, 1 << 20),
+                                       (5 * (1 << 20) + 3, 1 << 23)])   # the largest cache
+def test_exact_longest_history(L, max_len):
+    # 1M and 5M keys (the long-context lengths): 8 segments of ~131K / ~655K
+    # scores, each copied in many shared-memory slices; the second case in a
+    # cache of the largest supported max_len
     q, k, v = gauss(9, 1, 2, 1, L)
-    idx, out = run_exact(q, k, v, [L], 512, max_len=1 << 20)
+    idx, out = run_exact(q, k, v, [L], 512, max_len=max_len)
     from parity import support_ok
     for h in range(2):
         sup, kth, ref = oracle.exact_one(q[0, h], k[0, 0], v[0, 0], L, 512)
