@@ -14,11 +14,17 @@
 //      global candidate arrays.  The slice arrives in shared memory by one
 //      bulk copy (TMA) per 17K scores, issued before the histogram is read;
 //      every wait on it is bounded.
-//   2. Ranks exchange their counts through distributed shared memory; after a
-//      cluster barrier every rank gathers all candidates (from the peers'
-//      shared memory, or from global memory for a rank over kLocCap) and runs
-//      the same radix select on (score, lower index first) and stable
-//      compaction: identical ascending supports in every rank.
+//   2. Ranks exchange their counts and second-digit histograms through
+//      distributed shared memory; after a cluster barrier every rank knows the
+//      second digit T2 and each rank's number of final candidates (keys at or
+//      above the prefix (T1, T2)).  While every rank's candidates fit its
+//      shared memory, each rank pulls them (one warp per source rank);
+//      otherwise each rank compacts its own final candidates (from its shared
+//      memory, then its global segment) with all its threads and writes them
+//      into every rank's staging list at its offset, followed by a second
+//      cluster barrier.  Every rank then runs the same radix select on
+//      (score, lower index first) and stable compaction: identical ascending
+//      supports in every rank.
 //   3. Each rank aggregates 1/kExactCluster of the support's V rows with the
 //      common max and pushes (weighted sum, sum of weights) to rank 0, which
 //      normalises, writes the output and -- on decode / init -- inserts
@@ -382,13 +388,19 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     const int32_t *gi = w.cand_idx + (size_t)bh * w.cand_stride;
     const uint32_t *gk = w.cand_key + (size_t)bh * w.cand_stride;
     const bool staged = N2 <= kSelStageCap;
-    if (staged && warp < kExactCluster) {
-        // warp r gathers rank r's final candidates in order: from its shared
-        // memory when they all fit there, else from its global segment
+    // Every rank's candidates in its shared memory: warp r of each rank pulls
+    // rank r's final candidates in order.  Some rank past kLocCap (long
+    // histories): each rank pushes its own, compacted by all its threads.
+    int cmax = 0;
+#pragma unroll
+    for (int r = 0; r < kExactCluster; ++r)
+        cmax = max(cmax, sh.cnt[r]);
+    const bool push = cmax > kLocCap;
+    if (staged && !push && warp < kExactCluster) {
+        // warp r gathers rank r's final candidates in order from its shared memory
         const int r = warp, cr = sh.cnt[r];
-        const bool local = cr <= kLocCap;
-        const int32_t *pi = local ? cluster.map_shared_rank(loc_i, r) : gi + (size_t)r * seg;
-        const uint32_t *pk = local ? cluster.map_shared_rank(loc_k, r) : gk + (size_t)r * seg;
+        const int32_t *pi = cluster.map_shared_rank(loc_i, r);
+        const uint32_t *pk = cluster.map_shared_rank(loc_k, r);
         const unsigned lt = (1u << lane) - 1u;
         int dst = sh.off[r];
         uint32_t km = 0u;   // the largest key: the support's maximum (Eq. (12)'s shift)
@@ -417,9 +429,58 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
         if (lane == 0)
             atomicMax(&sh.kmax, km);
     }
-    if (staged)
+    if (staged && !push)
         for (int i = tid; i < 512; i += kSelThreads)
             (&sh.sel.hist[0][0])[i] = 0u;
+    if (staged && push) {
+        // this rank compacts its own final candidates (stable, all threads; the
+        // first kLocCap from shared memory, the rest from its global segment)
+        // and writes them into every rank's staging list at off[rank]
+        const int cr = sh.cnt[rank], o0 = sh.off[rank], o1 = sh.off[rank + 1];
+        int got = 0;
+        for (int base = 0; base < cr; base += kSelThreads * 4) {   // block-uniform trip count
+            const int j0 = base + tid * 4;
+            int32_t ii[4];
+            uint32_t kk[4];
+            int c = 0;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u;
+                ii[u] = 0;
+                kk[u] = 0u;
+                if (j < cr) {
+                    ii[u] = j < kLocCap ? loc_i[j] : oi[j];
+                    kk[u] = j < kLocCap ? loc_k[j] : ok[j];
+                    c += (kk[u] >> kSub) >= p19;
+                }
+            }
+            int total;
+            int d = o0 + got + block_excl_scan<kSelThreads>(c, sh.sel.warp_tot, total);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (j0 + u < cr && (kk[u] >> kSub) >= p19) {
+                    if (d < o1) {   // the histogram's count bounds the rank's range
+#pragma unroll
+                        for (int r2 = 0; r2 < kExactCluster; ++r2) {
+                            cluster.map_shared_rank(st_idx, r2)[d] = ii[u];
+                            cluster.map_shared_rank(st_key, r2)[d] = kk[u];
+                        }
+                    }
+                    ++d;
+                }
+            }
+            got += total;
+        }
+        for (int i = tid; i < 512; i += kSelThreads)
+            (&sh.sel.hist[0][0])[i] = 0u;
+        cluster.sync();   // every rank's final candidates are staged in every rank
+        uint32_t km = 0u;   // the largest key: the support's maximum (Eq. (12)'s shift)
+        for (int j = tid; j < N2; j += kSelThreads)
+            km = max(km, st_key[j]);
+        km = __reduce_max_sync(0xffffffffu, km);
+        if (lane == 0)
+            atomicMax(&sh.kmax, km);
+    }
     __syncthreads();
     auto goff = [&](int j) {
         int r = 0;
