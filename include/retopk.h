@@ -171,8 +171,8 @@ int retopk_decode_step_kv(retopk_ctx *ctx, const retopk_bf16 *k_new, const retop
  * which is then copied to `out`.  The first call allocates the staging
  * (pinned: 2 B Hq d * 2 + 2 B Hkv d * 2 bytes; device: 2 B Hq d bytes),
  * freed by retopk_destroy.  Not to be called from several threads on one
- * context, nor during stream capture.  Same results as retopk_decode_step_kv
- * on the same inputs. */
+ * context; on a capturing stream it returns RETOPK_ERR_INVALID.  Same
+ * results as retopk_decode_step_kv on the same inputs. */
 int retopk_decode_step_host(retopk_ctx *ctx, const retopk_bf16 *k_new, const retopk_bf16 *v_new,
                             const retopk_bf16 *q, retopk_bf16 *k_cache, retopk_bf16 *v_cache,
                             int32_t *d_seqlens, retopk_bf16 *out, void *stream);

@@ -62,6 +62,7 @@ def test_config_validation_without_gpu(lib):
                                          None, None, None, 0, None) == -1
     assert lib.retopk_strerror(-2).decode().startswith("unsupported")
     assert lib.retopk_decode_step(None, None, None, None, None, None, None) == -1
+    assert lib.retopk_decode_step_host(None, None, None, None, None, None, None, None, None) == -1
 
 
 def test_workspace_scales_with_context():

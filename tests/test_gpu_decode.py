@@ -15,6 +15,7 @@ import torch
 import oracle
 from parity import compare_decode_step, out_close
 from top_sparse_attention_exact_gb300 import synth
+from top_sparse_attention_exact_gb300.retopk import RetopkError
 from top_sparse_attention_exact_gb300.runner import DecodeRun, ExactRun
 
 pytestmark = pytest.mark.gpu
@@ -209,6 +210,15 @@ def test_host_buffer_step_matches_device_step():
             assert np.array_equal(da[key], db[key]), (t, key)
     assert torch.equal(host_run.k_cache, dev_run.k_cache) and torch.equal(host_run.seqlens, dev_run.seqlens)
     assert host_run.ctx.retopk_get_status() == 0
+    # a synchronous host-buffer call refuses a capturing stream (and leaves the capture intact)
+    s, g = torch.cuda.Stream(), torch.cuda.CUDAGraph()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            with pytest.raises(RetopkError):
+                host_run.ctx.retopk_decode_step_host(kh[0], vh[0], qh[0], host_run.k_cache, host_run.v_cache,
+                                                     host_run.seqlens, out_h, s)
+    torch.cuda.synchronize()
 
 
 def test_tau_above_one_equals_exact_every_step():

@@ -494,6 +494,8 @@ int retopk_decode_step_host(retopk_ctx *ctx, const retopk_bf16 *k_new, const ret
     const Work &w = ctx->w;
     const size_t nq = (size_t)w.B * w.Hq * kD * 2, nkv = (size_t)w.B * w.Hkv * kD * 2;
     cudaStream_t st = (cudaStream_t)stream;
+    if (capturing(st))   // a synchronous call with host copies cannot be captured
+        return RETOPK_ERR_INVALID;
     cudaError_t ce = cudaSuccess;
     if (!h.pin) {
         auto up = [](size_t x) { return (x + kAlign - 1) / kAlign * kAlign; };
