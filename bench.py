@@ -406,7 +406,8 @@ def our_arm(args, w, rank, world, dist):
     # ---- Exact Top-K on the same inputs (clean graph) --------------------------
     ex = ExactRun(dr)
     ex.capture()
-    ex_ms = timed_steps(lambda t: None, ex.replay, timed_t, flush, stream)
+    # staging (q copy, length fill) before the events, as for the ReTopK step
+    ex_ms = timed_steps(ex.stage, lambda t: ex.graph.replay(), timed_t, flush, stream)
     us_exact = float(ex_ms.mean() * 1000.0)
 
     # ---- per-kernel breakdown: profiled graphs on a second trajectory ----------
@@ -426,7 +427,7 @@ def our_arm(args, w, rank, world, dist):
     retopk.profile_reset()
     exp = ExactRun(dp)
     exp.capture(profiled=True)
-    kern_exact = profiled_steps(lambda t: None, exp.replay, timed_t, flush)
+    kern_exact = profiled_steps(exp.stage, lambda t: exp.graph.replay(), timed_t, flush)
     retopk.profile_reset()
     del dp, exp
     # the same trajectory as the clean run (bit-identical replays): bucket the

@@ -142,9 +142,13 @@ class ExactRun:
         self.graph = g
         return g
 
-    def replay(self, t: int):
-        """Exact step for decode step t's query over the first L0 + t + 1 keys."""
+    def stage(self, t: int):
+        """Stages decode step t's query and length L0 + t + 1 for the graph."""
         self.q_buf.copy_(self.dr.q_dec[t])
         self.sl_buf.fill_(self.dr.w.L0 + t + 1)
+
+    def replay(self, t: int):
+        """Exact step for decode step t's query over the first L0 + t + 1 keys."""
+        self.stage(t)
         self.graph.replay()
         return self.out
