@@ -168,9 +168,9 @@ int retopk_decode_step_kv(retopk_ctx *ctx, const retopk_bf16 *k_new, const retop
  * d_seqlens change), the path-decision kernel reading the token's q, k_new,
  * v_new across the host link (and copying q to device memory for the later
  * kernels) and the back end writing the output rows into the mapped buffer,
- * which is then copied to `out`.  The first call allocates the staging
- * (pinned: 2 B Hq d * 2 + 2 B Hkv d * 2 bytes; device: 2 B Hq d bytes),
- * freed by retopk_destroy.  Not to be called from several threads on one
+ * which is then copied to `out`.  The first call allocates the pinned host
+ * staging (2 B Hq d * 2 + 2 B Hkv d * 2 bytes), freed by retopk_destroy; the
+ * device copy of q is part of the workspace (no device allocation).  Not to be called from several threads on one
  * context; on a capturing stream it returns RETOPK_ERR_INVALID.  Same
  * results as retopk_decode_step_kv on the same inputs. */
 int retopk_decode_step_host(retopk_ctx *ctx, const retopk_bf16 *k_new, const retopk_bf16 *v_new,

@@ -26,7 +26,6 @@ using namespace retopk;
 struct HostStep {
     unsigned char *pin;     // pinned, mapped: q | k_new | v_new | out
     unsigned char *pin_d;   // its device address
-    unsigned char *dev;     // device copy of q
     size_t o_k, o_v, o_out, bytes;
     cudaStream_t cap;       // capture stream
     cudaGraph_t graph;
@@ -132,7 +131,8 @@ size_t plan(const retopk_config &c, bool stateful, Work *w, char *base)
     x.sc_stride = (c.max_len + 15) & ~15;
     const size_t BH = (size_t)c.batch * c.n_q_heads;
     Layout L;
-    size_t o_fq = 0, o_fs = 0, o_fl = 0, o_seq = 0, o_snap = 0, o_cnt = 0, o_path = 0, o_rho = 0, o_topr = 0;
+    size_t o_fq = 0, o_fs = 0, o_fl = 0, o_seq = 0, o_snap = 0, o_cnt = 0, o_path = 0, o_rho = 0, o_topr = 0,
+           o_qs = 0;
     if (stateful) {
         o_fq = L.add(BH * c.C * kD * 2);
         o_fs = L.add(BH * c.C * c.K * 4);
@@ -143,6 +143,7 @@ size_t plan(const retopk_config &c, bool stateful, Work *w, char *base)
         o_path = L.add(BH * 4);
         o_rho = L.add(BH * 4);
         o_topr = L.add(BH * c.R * 4);
+        o_qs = L.add(BH * kD * 2);
     }
     const size_t o_M = L.add(BH * 4);
     const size_t o_ci = L.add(BH * x.cand_stride * 4);
@@ -164,6 +165,7 @@ size_t plan(const retopk_config &c, bool stateful, Work *w, char *base)
             x.path = (int32_t *)(base + o_path);
             x.rho_max = (float *)(base + o_rho);
             x.topR = (int32_t *)(base + o_topr);
+            x.q_stage = (uint16_t *)(base + o_qs);
         }
         x.M = (int32_t *)(base + o_M);
         x.cand_idx = (int32_t *)(base + o_ci);
@@ -363,8 +365,6 @@ void release_host_step(HostStep &h)
         cudaGraphDestroy(h.graph);
     if (h.cap)
         cudaStreamDestroy(h.cap);
-    if (h.dev)
-        cudaFree(h.dev);
     if (h.pin)
         cudaFreeHost(h.pin);
     memset(&h, 0, sizeof h);
@@ -507,8 +507,6 @@ int retopk_decode_step_host(retopk_ctx *ctx, const retopk_bf16 *k_new, const ret
         if (ce == cudaSuccess)
             ce = cudaHostGetDevicePointer((void **)&h.pin_d, h.pin, 0);
         if (ce == cudaSuccess)
-            ce = cudaMalloc((void **)&h.dev, nq);
-        if (ce == cudaSuccess)
             ce = cudaStreamCreateWithFlags(&h.cap, cudaStreamNonBlocking);
         if (ce != cudaSuccess) {
             release_host_step(h);
@@ -532,7 +530,7 @@ int retopk_decode_step_host(retopk_ctx *ctx, const retopk_bf16 *k_new, const ret
             return cuda_rc(ce);
         const int e = decode_step(ctx, (const retopk_bf16 *)(h.pin_d + h.o_k), (const retopk_bf16 *)(h.pin_d + h.o_v),
                                   (const retopk_bf16 *)h.pin_d, k_cache, v_cache, d_seqlens,
-                                  (retopk_bf16 *)(h.pin_d + h.o_out), h.cap, (retopk_bf16 *)h.dev);
+                                  (retopk_bf16 *)(h.pin_d + h.o_out), h.cap, w.q_stage);
         cudaGraph_t g = nullptr;
         ce = cudaStreamEndCapture(h.cap, &g);
         if (e) {

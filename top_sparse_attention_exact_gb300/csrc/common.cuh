@@ -49,6 +49,7 @@ struct Work {
     int32_t *path;       // [B*Hq] (NULL: every head takes the exact path)
     float *rho_max;      // [B*Hq]
     int32_t *topR;       // [B*Hq*R]
+    uint16_t *q_stage;   // [B*Hq*d] device copy of q for retopk_decode_step_host
     int32_t *M;          // [B*Hq]
     int32_t *cand_idx;   // [B*Hq*cand_stride]
     uint32_t *cand_key;  // [B*Hq*cand_stride]
