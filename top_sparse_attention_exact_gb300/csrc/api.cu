@@ -792,7 +792,7 @@ int exact_topk_attention_step(const retopk_bf16 *q, const retopk_bf16 *k_cache, 
     cudaStream_t st = (cudaStream_t)stream;
     QSrc qs{q, (long long)Hq * kD, kD};
     if ((e = cuda_rc(timed(RETOPK_PROF_CLEAR, st,
-                           [&] { return cudaMemsetAsync(w.hist, 0, (size_t)B * Hq * kHistBins * 4, st); }))))
+                           [&] { return launch_clear_words(w.hist, (size_t)B * Hq * kHistBins * 4, st); }))))
         return e;
     if ((e = run_scan(w, qs, k_cache, d_seqlens, 0, st)))
         return e;

@@ -231,6 +231,7 @@ cudaError_t launch_finish(const Work &w, const uint16_t *q, const uint16_t *k_ca
 cudaError_t launch_append(const Work &w, const uint16_t *k_new, const uint16_t *v_new,
                           uint16_t *k_cache, uint16_t *v_cache, int32_t *seqlens, cudaStream_t st);
 cudaError_t launch_init_done(const Work &w, cudaStream_t st);
+cudaError_t launch_clear_words(void *p, size_t bytes, cudaStream_t st);
 cudaError_t launch_selftest_wait(uint32_t *status, long long limit, cudaStream_t st);
 int scan_ctas_per_sm();
 

@@ -2,6 +2,8 @@
 // value rows (and advancing L on the device), and finishing the cache
 // initialisation (ReTopK paper, §Recall-Before-Rerank: the cache is
 // initialised from the final C prompt tokens).
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace retopk {
@@ -52,6 +54,23 @@ __global__ void init_done_kernel(int32_t *seq, unsigned long long *counters, int
         for (int i = 0; i < CNT_WORDS; ++i)
             counters[(size_t)b * CNT_WORDS + i] = 0ull;
     }
+}
+
+// Zeroes n4 uint4 words (the exact step's histograms); lets the scan that
+// follows start its set-up at once (it waits for this grid before its flush).
+__global__ void clear_words_kernel(uint4 *p, long long n4)
+{
+    pdl_trigger();
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x)
+        p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+cudaError_t launch_clear_words(void *p, size_t bytes, cudaStream_t st)
+{
+    const long long n4 = (long long)(bytes / 16);
+    const int blocks = (int)std::min<long long>(152, (n4 + 255) / 256);
+    clear_words_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(reinterpret_cast<uint4 *>(p), n4);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_init_done(const Work &w, cudaStream_t st)
