@@ -242,33 +242,31 @@ def fidelity_pass(w, arrays, dev, n_steps):
     ReTopK step the stateless exact step on the same query and caches gives
     the Exact Top-K support S_t and output; the library's fidelity kernel
     scores the step's support against it (the paper's "Attention-support
-    fidelity" criterion), and Eq. (2)'s overlap with the most similar cached
-    query and Eq. (3)'s coverage by the R retrieved supports are taken from
-    the exact supports of the steps those cache entries came from."""
+    fidelity" criterion), and its overlap kernel gives Eq. (2)'s Overlap with
+    the most similar cached query and Eq. (3)'s Coverage(R) by the R retrieved
+    entries, from the exact supports of the steps those entries came from."""
     import torch
+    from top_sparse_attention_exact_gb300 import retopk
     from top_sparse_attention_exact_gb300.runner import DecodeRun, ExactRun
     dr = DecodeRun(w, arrays=arrays, device=dev)
     ex = ExactRun(dr)
+    BH = w.B * w.Hq
     hist, rows = [], []
     for s in range(n_steps):
         dr.step(s)
         ex.step(dr.q_dec[s])
         m = dr.ctx.retopk_fidelity(dr.q_dec[s], dr.k_cache, ex.idx, ex.out, dr.out).cpu().numpy().reshape(-1, 4)
         d = dr.ctx.retopk_get_diagnostics()
-        S = ex.idx.cpu().numpy().reshape(w.B * w.Hq, w.K)
-        hist.append([set(x[x >= 0].tolist()) for x in S])
-        cov = np.full(w.B * w.Hq, np.nan)
-        ovl = np.full(w.B * w.Hq, np.nan)
+        hist.append(ex.idx.view(BH, w.K).clone())
+        cov = np.full(BH, np.nan)
+        ovl = np.full(BH, np.nan)
         if s >= w.C:   # every cache entry came from a decode step of this pass
-            for bh in range(w.B * w.Hq):
-                pos = [c for c in d["topR"][bh] if c >= 0]
-                steps = [s - w.C + c for c in pos]
-                if not steps:
-                    continue
-                St = hist[s][bh]
-                U = set().union(*(hist[j][bh] for j in steps))
-                cov[bh] = len(St & U) / max(1, len(St))
-                ovl[bh] = len(St & hist[steps[0]][bh]) / max(1, len(St))
+            topR = torch.from_numpy(d["topR"]).to(dev).long()          # [BH, R] live positions, -1 padded
+            H = torch.stack(hist[s - w.C:s], dim=1)                     # [BH, C, K] by live position
+            others = torch.gather(H, 1, topR.clamp(min=0)[:, :, None].expand(BH, w.R, w.K)).contiguous()
+            others[topR < 0] = -1
+            oc = retopk.support_overlap(hist[s], others).cpu().numpy()
+            ovl, cov = oc[:, 0], oc[:, 1]
         rows.append((d["path"].copy(), m, cov, ovl))
     del dr, ex
     torch.cuda.synchronize()
@@ -288,7 +286,7 @@ def fidelity_pass(w, arrays, dev, n_steps):
     return {"steps": n_steps, "reuse_path": summary(lambda r: r[0] == 0),
             "all_heads": summary(lambda r: np.ones_like(r[0], dtype=bool)),
             "how": "exact shadow (stateless exact step on the same q and caches) after each decode step; "
-                   "retopk_fidelity on the GPU; coverage/overlap from the shadow's exact supports"}
+                   "retopk_fidelity and retopk_support_overlap (Eqs. (2)-(3)) on the GPU"}
 
 
 def layers_pass(w, arrays, dev, n_layers, n_tokens, warm, flush, stream):
@@ -506,11 +504,9 @@ def our_arm(args, w, rank, world, dist):
     cpu = None
     if rank == 0 and not args.no_cpu:
         import oracle
-        sys.path.insert(0, os.path.join(ROOT, "tests"))
-        from parity import oracle_state_from_gpu
         oracle.build()
         oracle.set_threads(oracle_threads())
-        st = oracle_state_from_gpu(init_state, 0, wr.K)
+        st = oracle.state_from_export(init_state, 0, wr.K)
         n, secs = run_oracle_steps(wr, arrays, st, range(0, wr.steps), budget_s=args.cpu_budget)
         cpu = {"value": secs / n * 1e6, "unit": UNIT, "cores": oracle.get_threads(), "kind": "oracle",
                "sample": f"decode steps 1..{n} of sequence 0 from the GPU's initialised cache "

@@ -261,7 +261,11 @@ int exact_topk_attention_step(const retopk_bf16 *q, const retopk_bf16 *k_cache,
  *     overlap on the GPU (other streams, other threads) race on it.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
- * Every GPU that loads the library holds the 16 MiB until the process exits. */
+ *   - The 16 MiB are reserved on a device when the library's module is loaded
+ *     there.  Under CUDA's default lazy module loading that is this first
+ *     call, which can therefore return RETOPK_ERR_CUDA if the device has no
+ *     16 MiB left: make it at start-up.  From then on the device holds the
+ *     array until the process exits, and no later call takes device memory. */
 int exact_topk_attention_step_noalloc(const retopk_bf16 *q, const retopk_bf16 *k_cache,
                                       const retopk_bf16 *v_cache, const int32_t *d_seqlens,
                                       int B, int Hq, int Hkv, int d, int max_len, int K,
@@ -285,6 +289,18 @@ int exact_topk_attention_step_noalloc(const retopk_bf16 *q, const retopk_bf16 *k
  * [B, Hq, d] bf16.  A diagnostic beside the decode loop, not part of it. */
 int retopk_fidelity(retopk_ctx *ctx, const retopk_bf16 *q, const retopk_bf16 *k_cache, const int32_t *exact_idx,
                     const retopk_bf16 *out_exact, const retopk_bf16 *out, float *metrics, void *stream);
+
+/* Support overlap and coverage (ReTopK paper, §Motivation Eqs. (2)-(3)): for
+ * each of `rows` rows, S [rows, K] is a support (e.g. the Exact Top-K support
+ * S_t) and others [rows, R, K] the R supports it is compared with (e.g. the
+ * Exact Top-K supports of the R most similar preceding queries, most similar
+ * first); all ascending, -1 padded, device int32.  out: device float
+ * [rows, 2] = (|S n others[0]| / K  -- Eq. (2)'s Overlap with the most
+ * similar one --, |S n U| / K with U the union of the R supports -- Eq. (3)'s
+ * Coverage(R)).  1 <= R <= 256, 1 <= K <= 4096.  Asynchronous on `stream`;
+ * a diagnostic, not part of the decode step. */
+int retopk_support_overlap(const int32_t *S, const int32_t *others, int rows, int R, int K, float *out,
+                           void *stream);
 
 /* ---- profiling ----------------------------------------------------------- */
 

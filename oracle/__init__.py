@@ -70,6 +70,10 @@ def _declare(lib):
     lib.oracle_decode_step.argtypes = [_P, _P, _P, _L, _I, _I, _I, _I, _I, _I, _I, _I, _I, _D, _I,
                                        _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P]
     lib.oracle_fidelity.argtypes = [_P, _P, _L, _I, _P, _I, _P, _I, _P, _P, _P]
+    lib.oracle_overlap.argtypes = [_P, _I, _P, _I, _I]
+    lib.oracle_overlap.restype = _D
+    lib.oracle_coverage.argtypes = [_P, _P, _P, _P, _I, _I, _I, _P, _I, _I, _P]
+    lib.oracle_coverage.restype = _D
     lib.oracle_set_threads.argtypes = [_I]
     lib.oracle_get_threads.restype = _I
     return lib
@@ -107,6 +111,45 @@ def fidelity(q, k, S, Sh, o, oh, lib=None):
     lib.oracle_fidelity(_p(q), _p(k), k.shape[-1], q.shape[-1], _p(S), len(S), _p(Sh), len(Sh), _p(o), _p(oh),
                         _p(out))
     return out
+
+
+def overlap(St, Sj, K, lib=None):
+    """Eq. (2): |S_t n S_j| / K for two ascending supports (-1 entries ignored)."""
+    lib = lib or load()
+    St = _i32(np.asarray(St)[np.asarray(St) >= 0])
+    Sj = _i32(np.asarray(Sj)[np.asarray(Sj) >= 0])
+    return float(lib.oracle_overlap(_p(St), len(St), _p(Sj), len(Sj), int(K)))
+
+
+def coverage(q, prev_q, prev_S, St, R, K, lib=None):
+    """Eq. (3): coverage of St by the union of the supports of the R preceding
+    queries most similar to q.  prev_q [n, d] oldest first, prev_S a list of n
+    ascending supports.  Returns (coverage, chosen positions [R], -1 padded)."""
+    lib = lib or load()
+    q = _u16(q)
+    prev_q = _u16(prev_q).reshape(-1, q.shape[-1])
+    n, d = prev_q.shape
+    sups = [_i32(np.asarray(s)[np.asarray(s) >= 0]) for s in prev_S]
+    assert len(sups) == n
+    qp = (ctypes.c_void_p * max(n, 1))(*[prev_q[c].ctypes.data for c in range(n)])
+    sp = (ctypes.c_void_p * max(n, 1))(*[s.ctypes.data for s in sups])
+    ln = _i32([len(s) for s in sups] or [0])
+    St = _i32(np.asarray(St)[np.asarray(St) >= 0])
+    chosen = np.empty(max(R, 1), dtype=np.int32)
+    cov = lib.oracle_coverage(_p(q), qp, sp, _p(ln), n, d, int(R), _p(St), len(St), int(K), _p(chosen))
+    return float(cov), chosen[:R].copy()
+
+
+def state_from_export(st: dict, b: int, K: int) -> "CacheState":
+    """The oracle's cache state for sequence b from a library state export
+    (the dict of arrays the binding's retopk_export_state returns)."""
+    Hq, C, d = st["fifo_q"].shape[1], st["fifo_q"].shape[2], st["fifo_q"].shape[3]
+    cs = CacheState(Hq, C, K, d)
+    cs.fq[...] = st["fifo_q"][b]
+    cs.fsup[...] = st["fifo_sup"][b]
+    cs.flen[...] = st["fifo_len"][b]
+    cs.seq[...] = st["seq"][b]
+    return cs
 
 
 def set_threads(n: int) -> None:

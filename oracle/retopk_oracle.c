@@ -9,7 +9,9 @@
  * Method: "Recall Before You Rank: Similarity-Guided Top-K Reuse for Efficient
  * Long-Context Attention" (ReTopK).  Each function names the equation it
  * follows; sections are those of that paper:
- *   §Motivation               Eq. (1)  Exact Top-K support
+ *   §Motivation               Eq. (1)  Exact Top-K support;
+ *                             Eqs. (2)-(3) support overlap and coverage
+ *                                        (diagnostics of support reuse)
  *   §Problem Setup            Eq. (4)  full-history scores
  *   §Recall-Before-Rerank     Eqs. (5)-(12)  cache, recall, candidates,
  *                                        rerank, reranked support, sparse
@@ -496,6 +498,55 @@ void oracle_fidelity(const uint16_t *q, const uint16_t *k, int64_t ld, int d,
     out[3] = (p2 > 0.0 && ph2 > 0.0) ? cross / (sqrt(p2) * sqrt(ph2)) : 0.0;
     free(eS);
     free(eh);
+}
+
+/* §Motivation Eq. (2): the normalised overlap of two Exact Top-K supports,
+ * |S_t n S_j| / K (both ascending; the denominator is K as printed, also when
+ * a support is shorter than K because fewer keys exist). */
+double oracle_overlap(const int32_t *St, int nt, const int32_t *Sj, int nj, int K)
+{
+    int common = 0;
+    for (int a = 0, b = 0; a < nt && b < nj;) {
+        if (St[a] < Sj[b])
+            ++a;
+        else if (Sj[b] < St[a])
+            ++b;
+        else {
+            ++common;
+            ++a;
+            ++b;
+        }
+    }
+    return (double)common / K;
+}
+
+/* §Motivation Eq. (3): Coverage_t(R) = |S_t n U_t(R)| / K, where U_t(R) is the
+ * union of the supports of the R preceding queries most similar to q (cosine,
+ * Eq. (6); ties to the older query, as for Eq. (7)).  prev_q / prev_S /
+ * prev_n: the n_prev preceding queries, oldest first, with their ascending
+ * supports.  chosen[0..R) receives the selected positions (-1 padded).
+ * Returns the coverage. */
+double oracle_coverage(const uint16_t *q, const uint16_t *const *prev_q, const int32_t *const *prev_S,
+                       const int32_t *prev_n, int n_prev, int d, int R, const int32_t *St, int nt, int K,
+                       int32_t *chosen)
+{
+    double *rho = (double *)malloc(sizeof(double) * (size_t)(n_prev > 0 ? n_prev : 1));
+    oracle_recall(q, prev_q, n_prev, d, R, rho, chosen);
+    const int m = n_prev < R ? n_prev : R;
+    const int32_t *sp[256];
+    int32_t ln[256];
+    int total = 0;
+    for (int r = 0; r < m && r < 256; ++r) {
+        sp[r] = prev_S[chosen[r]];
+        ln[r] = prev_n[chosen[r]];
+        total += ln[r];
+    }
+    int32_t *U = (int32_t *)malloc(sizeof(int32_t) * (size_t)(total > 0 ? total : 1));
+    const int nu = oracle_candidates(sp, ln, m < 256 ? m : 256, 0, 0, U);   /* union only: no window */
+    const double cov = oracle_overlap(St, nt, U, nu, K);
+    free(U);
+    free(rho);
+    return cov;
 }
 
 void oracle_set_threads(int n)

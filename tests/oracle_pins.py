@@ -379,8 +379,109 @@ def pin_fidelity(lib):
     assert m[0] == 0.0 and m[1] == 0.0 and m[3] == 0.0 and abs(m[2] + 1.0) < 1e-12, m
 
 
+def pin_exact_step_batched(lib):
+    """The batched Exact Top-K step (Eqs. (1), (4), (12)) against brute force
+    per (sequence, query head): ragged lengths (one shorter than K), query
+    head h reading KV head h // G of its own sequence, -1 padding past the
+    support, the K-th score."""
+    rng = np.random.default_rng(21)
+    B, Hq, Hkv, T, d, K = 2, 4, 2, 70, 128, 9
+    G = Hq // Hkv
+    q = _bf(rng.standard_normal((B, Hq, d)))
+    k = _bf(rng.standard_normal((B, Hkv, T, d)))
+    v = _bf(rng.standard_normal((B, Hkv, T, d)))
+    L = np.array([70, 6], np.int32)
+    sup, sup_len, kth, out = oracle.exact_step(q, k, v, L, K, lib=lib)
+    for b in range(B):
+        for h in range(Hq):
+            want_sup, want_out = _brute_exact(q[b, h], k[b, h // G], v[b, h // G], int(L[b]), K)
+            n = int(sup_len[b, h])
+            assert sup[b, h, :n].tolist() == want_sup, (b, h)
+            assert (sup[b, h, n:] == -1).all(), (b, h)
+            assert np.allclose(out[b, h], want_out, rtol=0, atol=1e-12), (b, h)
+            s = _f(k[b, h // G, :L[b]]) @ _f(q[b, h]) / math.sqrt(d)
+            assert abs(kth[b, h] - np.sort(s)[::-1][min(K, int(L[b])) - 1]) < 1e-12, (b, h)
+
+
+def pin_attention_on_support_numpy(lib):
+    """Eqs. (10) + (12) on a given support (unsorted, arbitrary rows): a numpy
+    float64 softmax over the gathered K rows weighting the gathered V rows."""
+    rng = np.random.default_rng(22)
+    d = 128
+    q = _bf(rng.standard_normal(d))
+    k = _bf(rng.standard_normal((50, d)))
+    v = _bf(rng.standard_normal((50, d)))
+    for sup in ([3, 17, 4, 49, 0, 22], [31], list(range(50))):
+        sup = np.array(sup, np.int32)
+        s = _f(k)[sup] @ _f(q) / math.sqrt(d)
+        w = np.exp(s - s.max())
+        ref = (w / w.sum()) @ _f(v)[sup]
+        got = oracle.attention_on_support(q, k, v, sup, lib=lib)
+        assert np.allclose(got, ref, rtol=0, atol=1e-13), sup
+
+
+def pin_overlap_coverage(lib):
+    """Eq. (2) against Python set arithmetic (denominator K, also for a
+    support shorter than K) and Eq. (3) with preceding queries whose cosines
+    to q are known in closed form, so the R most similar are fixed."""
+    rng = np.random.default_rng(23)
+    assert oracle.overlap([1, 2, 3, 4], [3, 4, 5, 6], 4, lib=lib) == 0.5
+    assert oracle.overlap([0, 1], [1], 4, lib=lib) == 0.25
+    for trial in range(30):
+        K = int(rng.integers(1, 40))
+        L = int(rng.integers(1, 80))
+        a = np.sort(rng.choice(L, min(K, L), replace=False))
+        b = np.sort(rng.choice(L, min(K, L), replace=False))
+        assert oracle.overlap(a, b, K, lib=lib) == len(set(a.tolist()) & set(b.tolist())) / K
+    q = _bf([1, 0, 0, 0])
+    prev_q = _bf([[0, 1, 0, 0],      # cosine 0, oldest
+                  [2, 0, 0, 0],      # 1
+                  [-1, 0, 0, 0],     # -1
+                  [1, 1, 0, 0],      # 1/sqrt(2)
+                  [0, 0, 3, 0]])     # 0, newest
+    prev_S = [[0, 1, 2], [10, 11, 12, 13], [20, 21], [12, 13, 14, 30], [40, 41]]
+    St = [0, 11, 13, 14, 20, 30, 41, 50]
+    K = 8
+    for R, want in ((1, [1]), (2, [1, 3]), (3, [1, 3, 0]), (4, [1, 3, 0, 4]), (6, [1, 3, 0, 4, 2, -1])):
+        cov, chosen = oracle.coverage(q, prev_q, prev_S, St, R, K, lib=lib)
+        assert chosen.tolist() == want, (R, chosen)
+        U = set().union(*[set(prev_S[c]) for c in want if c >= 0])
+        assert cov == len(set(St) & U) / K, (R, cov)
+
+
+def pin_window_zero_and_no_fallback(lib):
+    """The W = 0 and tau = -inf ablations (Table 3): every step reuses (no
+    cosine is below -inf), the candidate set is exactly the union of the
+    retrieved entries' supports with no recent window, and the support and
+    output are the brute-force Top-K and softmax over that set."""
+    Hq, Hkv, K, C, L0, R = 4, 2, 8, 6, 96, 2
+    G = Hq // Hkv
+    k, v, qp, qd = _small_workload(24, L0=L0, Hq=Hq, Hkv=Hkv, K=K, C=C)
+    st = oracle.init_cache(qp, k, L0, Hq, Hkv, K, C, lib=lib)
+    for t in range(len(qd)):
+        L = L0 + t + 1
+        pre = st.copy()
+        r = oracle.decode_step(st, qd[t], k, v, L, Hkv, 0, R, 0, -math.inf, lib=lib)
+        assert (r["path"] == 0).all(), (t, r["path"])
+        for h in range(Hq):
+            live = pre.live(h)
+            qh = _f(qd[t, h])
+            cos = [float(_f(x) @ qh / (np.linalg.norm(_f(x)) * np.linalg.norm(qh))) for x, _ in live]
+            top = sorted(range(len(live)), key=lambda c: (-cos[c], c))[:R]
+            A = sorted(set().union(*[set(live[c][1].tolist()) for c in top]))
+            assert r["cand"][h, :r["M"][h]].tolist() == A, (t, h)
+            s = _f(k[h // G])[A] @ qh / math.sqrt(128)
+            order = sorted(range(len(A)), key=lambda j: (-s[j], A[j]))[:K]
+            sup = sorted(A[j] for j in order)
+            assert r["sup"][h, :r["sup_len"][h]].tolist() == sup, (t, h)
+            ss = _f(k[h // G])[sup] @ qh / math.sqrt(128)
+            w = np.exp(ss - ss.max())
+            assert np.allclose(r["out"][h], (w / w.sum()) @ _f(v[h // G])[sup], rtol=0, atol=1e-12), (t, h)
+
+
 ALL_PINS = [pin_hand_worked_exact, pin_hand_worked_reuse, pin_scores_library_and_closed_form,
             pin_topk_brute_force, pin_softmax_closed_forms, pin_dense_equals_sdpa,
             pin_softmax_merge, pin_recall_closed_forms, pin_candidates_set_union,
             pin_init_cache_causal, pin_degenerate_paths, pin_rerank_recovers_exact,
-            pin_fifo_contents, pin_fidelity, pin_recent_retrieval]
+            pin_fifo_contents, pin_fidelity, pin_recent_retrieval, pin_exact_step_batched,
+            pin_attention_on_support_numpy, pin_overlap_coverage, pin_window_zero_and_no_fallback]

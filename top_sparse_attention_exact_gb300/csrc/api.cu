@@ -5,6 +5,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -70,32 +71,51 @@ int cuda_rc(cudaError_t e)
     return RETOPK_ERR_CUDA;
 }
 
+// Both the SM count and the kernels' attributes (cudaFuncSetAttribute) belong
+// to a device: they are kept per device, for the device current at the call.
+constexpr int kMaxDevices = 64;
+
+int current_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return -1;
+    return dev;
+}
+
 int sm_count()
 {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
-            n = 1;
+    static std::atomic<int> n[kMaxDevices];
+    const int dev = current_device();
+    if (dev < 0)
+        return 1;
+    int v = n[dev].load(std::memory_order_relaxed);
+    if (!v) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1)
+            v = 1;
+        n[dev].store(v, std::memory_order_relaxed);
     }
-    return n;
+    return v;
 }
 
 int ensure_configured()
 {
-    static std::once_flag once;
-    static cudaError_t err = cudaSuccess;
-    std::call_once(once, [] {
-        err = configure_scan();
-        if (err == cudaSuccess)
-            err = configure_select();
-        if (err == cudaSuccess)
-            err = configure_finish();
-        if (err == cudaSuccess)
-            err = configure_fidelity();
+    static std::once_flag once[kMaxDevices];
+    static cudaError_t err[kMaxDevices];
+    const int dev = current_device();
+    if (dev < 0)
+        return RETOPK_ERR_UNSUPPORTED;
+    std::call_once(once[dev], [dev] {
+        cudaError_t e = configure_scan();
+        if (e == cudaSuccess)
+            e = configure_select();
+        if (e == cudaSuccess)
+            e = configure_finish();
+        if (e == cudaSuccess)
+            e = configure_fidelity();
+        err[dev] = e;
     });
-    return cuda_rc(err);
+    return cuda_rc(err[dev]);
 }
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
@@ -292,7 +312,6 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratch
 // device (with that device current) on the first call made there.
 int noalloc_scratch(void **out)
 {
-    constexpr int kMaxDevices = 64;
     static std::mutex mu;
     static void *addr[kMaxDevices] = {};
     int dev = 0;
@@ -573,6 +592,14 @@ int retopk_fidelity(retopk_ctx *ctx, const retopk_bf16 *q, const retopk_bf16 *k_
     const Work &w = ctx->w;
     return cuda_rc(launch_fidelity(q, k_cache, exact_idx, w.support, out_exact, out, metrics, w.B, w.Hq, w.Hkv,
                                    w.max_len, w.K, (cudaStream_t)stream));
+}
+
+int retopk_support_overlap(const int32_t *S, const int32_t *others, int rows, int R, int K, float *out,
+                           void *stream)
+{
+    if (!S || !others || !out || rows < 1 || R < 1 || R > kMaxC || K < 1 || K > kMaxK)
+        return RETOPK_ERR_INVALID;
+    return cuda_rc(launch_overlap(S, others, rows, R, K, out, (cudaStream_t)stream));
 }
 
 int retopk_get_diagnostics(retopk_ctx *ctx, int32_t *path, float *rho_max, int32_t *topR, int32_t *M,

@@ -223,6 +223,8 @@ cudaError_t launch_exact_select(const Work &w, QSrc q, const uint16_t *v_cache, 
 cudaError_t launch_fidelity(const uint16_t *q, const uint16_t *k, const int32_t *S, const int32_t *Sh,
                             const uint16_t *o, const uint16_t *oh, float *out, int B, int Hq, int Hkv,
                             int max_len, int K, cudaStream_t st);
+cudaError_t launch_overlap(const int32_t *S, const int32_t *others, int rows, int R, int K, float *out,
+                           cudaStream_t st);
 cudaError_t launch_decide(const Work &w, const uint16_t *q, uint16_t *q_copy, const uint16_t *k_new,
                           const uint16_t *v_new, uint16_t *k_cache, uint16_t *v_cache, int32_t *seqlens,
                           cudaStream_t st);

@@ -181,6 +181,85 @@ cudaError_t launch_fidelity(const uint16_t *q, const uint16_t *k, const int32_t 
     return cudaGetLastError();
 }
 
+// ---- support overlap and coverage (§Motivation Eqs. (2)-(3)) ----------------
+// One CTA per row: S [rows, K] and the R supports others [rows, R, K], each
+// ascending and -1 padded.  out[row] = (Overlap(S, others[0]),
+// Coverage(S, union of others)), both over K.  Membership is a binary search
+// over the valid prefix of each list; the union is never materialised.
+constexpr int kOvThreads = 256;
+
+__device__ __forceinline__ int valid_len(const int32_t *s, int K)
+{
+    int lo = 0, hi = K;   // entries >= 0 come first, then the -1 padding
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (s[mid] >= 0)
+            lo = mid + 1;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ bool contains(const int32_t *s, int n, int32_t x)
+{
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (s[mid] < x)
+            lo = mid + 1;
+        else
+            hi = mid;
+    }
+    return lo < n && s[lo] == x;
+}
+
+__global__ void __launch_bounds__(kOvThreads) overlap_kernel(const int32_t *S, const int32_t *others, int R, int K,
+                                                             float *out)
+{
+    __shared__ int lens[kMaxC + 1];
+    __shared__ int cnt[2][kOvThreads / 32];
+    const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int32_t *s = S + (size_t)row * K;
+    const int32_t *o = others + (size_t)row * R * K;
+    for (int r = tid; r <= R; r += kOvThreads)
+        lens[r] = valid_len(r < R ? o + (size_t)r * K : s, K);
+    __syncthreads();
+    const int ns = lens[R];
+    int first = 0, any = 0;
+    for (int j = tid; j < ns; j += kOvThreads) {
+        const int32_t x = s[j];
+        bool in_first = false, in_any = false;
+        for (int r = 0; r < R && !in_any; ++r) {
+            const bool c = contains(o + (size_t)r * K, lens[r], x);
+            in_first |= (r == 0) && c;
+            in_any |= c;
+        }
+        first += in_first;
+        any += in_any;
+    }
+    first = warp_isum(first);
+    any = warp_isum(any);
+    if (lane == 0) {
+        cnt[0][warp] = first;
+        cnt[1][warp] = any;
+    }
+    __syncthreads();
+    if (tid < 2) {
+        int c = 0;
+        for (int i = 0; i < kOvThreads / 32; ++i)
+            c += cnt[tid][i];
+        out[(size_t)row * 2 + tid] = (float)c / (float)K;
+    }
+}
+
+cudaError_t launch_overlap(const int32_t *S, const int32_t *others, int rows, int R, int K, float *out,
+                           cudaStream_t st)
+{
+    overlap_kernel<<<rows, kOvThreads, 0, st>>>(S, others, R, K, out);
+    return cudaGetLastError();
+}
+
 cudaError_t configure_fidelity()
 {
     return cudaFuncSetAttribute(fidelity_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxK * 16);

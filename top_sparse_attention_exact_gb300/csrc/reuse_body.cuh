@@ -316,6 +316,7 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
         const int hw = tid >> 4, hl = tid & 15;
         const float *qq = sh.qf + hl * 8;
         const uint16_t *kb = a.k + ((size_t)(b * w.Hkv + hk) * w.max_len) * kD;
+        bool nonfinite = false;
         for (int jb = cs; jb < ce; jb += kHalfWarps * kRerankRows) {
             uint4 kv[kRerankRows];
 #pragma unroll
@@ -333,10 +334,15 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
                 for (int o = 8; o > 0; o >>= 1)
                     s += __shfl_xor_sync(0xffffffffu, s, o);
                 const int j = jb + hw + u * kHalfWarps;
-                if (hl == 0 && j < ce)
-                    keys[j] = f2key(s * a.scale + 0.0f);
+                if (hl == 0 && j < ce) {
+                    const float sc = s * a.scale + 0.0f;
+                    nonfinite |= !(fabsf(sc) <= 3.402823466e38f);
+                    keys[j] = f2key(sc);
+                }
             }
         }
+        if (nonfinite)
+            atomicOr(w.status, RETOPK_STATUS_NONFINITE);
     }
     __syncthreads();   // the slice's scores are written
     // push the slice into every peer (each is past its bitmap: cluster barrier above)

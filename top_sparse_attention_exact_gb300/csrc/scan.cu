@@ -226,6 +226,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         int b = 0, hk = 0, L = 0;
         uint4 qf[NT][4];
         bool ok = true;
+        bool nonfinite = false;   // a score that is NaN or +-inf (reported once per thread)
         for (int it = 0, tile = t_begin; tile < t_end; ++it, ++tile) {
             int ng = gi < 0 ? 0 : gi;
             while (tile >= sh.grp_first[ng + 1])
@@ -305,6 +306,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                     const int r = (e < 2) ? r0 : r1;
                     if (n < G && r < L && ((mask >> n) & 1u)) {
                         const float sc = c[nt][e] * a.scale + 0.0f;
+                        nonfinite |= !(fabsf(sc) <= 3.402823466e38f);
                         st_keep(&sc_base[(size_t)n * a.sc_stride + r], sc, keep);
                         atomicAdd(&hist_s[n * kHistBins + (f2key(sc) >> (32 - kHistBits))], 1u);
                     }
@@ -314,6 +316,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         consumer_sync();
         if (gi >= 0)
             flush_hist(hist_s, a.hist + (size_t)(b * a.Hq + hk * G) * kHistBins, G, mask, tid);
+        if (nonfinite)
+            atomicOr(a.status, RETOPK_STATUS_NONFINITE);
     }
     __syncthreads();
     // Drain: every issued copy has landed before shared memory is released

@@ -28,7 +28,7 @@ EXPORTED = ("retopk_workspace_bytes", "retopk_create", "retopk_destroy", "retopk
             "exact_topk_workspace_bytes", "exact_topk_attention_step",
             "retopk_profile_enable", "retopk_profile_read", "retopk_profile_reset",
             "retopk_selftest_wait", "exact_topk_attention_step_noalloc", "retopk_fidelity",
-            "retopk_decode_step_host")
+            "retopk_decode_step_host", "retopk_support_overlap")
 
 PROF_KERNELS = ("append", "finish", "scan", "select", "clear", "decide")
 
@@ -79,6 +79,7 @@ def _declare(lib):
     lib.retopk_profile_reset.argtypes = []
     lib.retopk_selftest_wait.argtypes = [_P, ctypes.c_int64, _P]
     lib.exact_topk_attention_step_noalloc.argtypes = [_P, _P, _P, _P] + [_I] * 6 + [_P, _P, _P]
+    lib.retopk_support_overlap.argtypes = [_P, _P, _I, _I, _I, _P, _P]
     for name in EXPORTED:
         getattr(lib, name).restype = getattr(lib, name).restype or ctypes.c_int
     return lib
@@ -179,6 +180,20 @@ def exact_topk_attention_step_noalloc(q, k_cache, v_cache, seqlens, K, out, idx_
         _ptr(_bf16(q)), _ptr(_bf16(k_cache)), _ptr(_bf16(v_cache)), _ptr(_i32(seqlens)), B, Hq, Hkv, d,
         max_len, int(K), _ptr(_bf16(out)), _ptr(idx_out) if idx_out is not None else None, _stream(stream))
     _check(rc, "exact_topk_attention_step_noalloc")
+    return out
+
+
+def support_overlap(S, others, stream=None):
+    """Eqs. (2)-(3): S [rows, K] and others [rows, R, K] int32 CUDA tensors
+    (ascending, -1 padded) -> float32 CUDA tensor [rows, 2] = (overlap with
+    others[:, 0], coverage by the union of the R)."""
+    rows, K = S.shape
+    R = others.shape[1]
+    if tuple(others.shape) != (rows, R, K):
+        raise RetopkError(f"others must be [rows, R, K], got {tuple(others.shape)}")
+    out = torch.empty((rows, 2), dtype=torch.float32, device=S.device)
+    _check(load().retopk_support_overlap(_ptr(_i32(S)), _ptr(_i32(others)), rows, R, K, _ptr(out), _stream(stream)),
+           "retopk_support_overlap")
     return out
 
 
