@@ -18,6 +18,11 @@ Tolerances (written here, applied everywhere):
   * outputs: max-abs <= 2e-2 and relative L2 <= 1e-2 against the oracle's
     fp64 Eq. (12) output on the GPU's own support, and separately against the
     oracle's output on the oracle's own support (whenever path and R_t agree).
+    Where the two supports differ by legal near-tie swaps, a swap changes the
+    output by the swapped keys' own contributions, which can exceed 1e-2 of a
+    small output's norm; the second comparison then allows, on top of the
+    tolerance, the relative difference the swaps alone cause (the oracle's
+    fp64 outputs on the two supports, compared with each other).
 Band exemptions are counted and returned, so the tests can report and bound
 them.
 """
@@ -44,6 +49,22 @@ def out_close(got: np.ndarray, ref: np.ndarray):
     mx = float(np.abs(got - ref).max()) if got.size else 0.0
     rel = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
     return (mx <= OUT_MAX_ABS and rel <= OUT_REL_L2), mx, rel
+
+
+def out_close_swapped(got, ref_own, ref_gpu_support):
+    """Output check against the oracle's output on its own support (ref_own),
+    when the GPU's support may differ from it by legal near-tie swaps:
+    max-abs <= OUT_MAX_ABS, and relative L2 <= OUT_REL_L2 plus the relative
+    difference between the oracle's fp64 outputs on the two supports
+    (ref_gpu_support is the oracle's output on the GPU's support; 0 when the
+    supports are equal)."""
+    ref_own = np.asarray(ref_own, np.float64)
+    swap = float(np.linalg.norm(np.asarray(ref_gpu_support, np.float64) - ref_own) /
+                 max(np.linalg.norm(ref_own), 1e-30))
+    got = np.asarray(got, np.float64)
+    mx = float(np.abs(got - ref_own).max()) if got.size else 0.0
+    rel = float(np.linalg.norm(got - ref_own) / max(np.linalg.norm(ref_own), 1e-30))
+    return (mx <= OUT_MAX_ABS and rel <= OUT_REL_L2 + swap), mx, rel
 
 
 def support_ok(q, k_rows, got, want, kth):
@@ -89,7 +110,7 @@ def compare_exact(q, k, v, L, K, gpu_idx, gpu_out, where=""):
             ok, mx, rel = out_close(gpu_out[b, h], ref)
             if not ok:
                 errs.append(f"{where} b{b} h{h}: out max {mx:.3g} rel {rel:.3g}")
-            ok, mx, rel = out_close(gpu_out[b, h], out[b, h])
+            ok, mx, rel = out_close_swapped(gpu_out[b, h], out[b, h], ref)
             if not ok:
                 errs.append(f"{where} b{b} h{h}: out vs oracle support max {mx:.3g} rel {rel:.3g}")
     return errs
@@ -180,7 +201,7 @@ def compare_decode_step(pre: dict, post: dict, diag: dict, q_t, k, v, L, w, gpu_
                 errs.append(f"{tag}: out max {mx:.3g}/{mx2:.3g} rel {rel:.3g}/{rel2:.3g}")
             if topR_same:
                 # separately: against the oracle's output on the oracle's own support
-                ok3, mx3, rel3 = out_close(got_bf16, r["out"][h])
+                ok3, mx3, rel3 = out_close_swapped(got_bf16, r["out"][h], ref)
                 if not ok3:
                     errs.append(f"{tag}: out vs oracle support max {mx3:.3g} rel {rel3:.3g}")
             # the cache slot written by this step

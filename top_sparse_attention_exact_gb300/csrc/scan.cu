@@ -27,8 +27,9 @@
 //
 // Epilogue: fp32 scores go to the workspace, and an 11-bit histogram of
 // their order-preserving keys is kept per exact head in shared memory and
-// flushed to global memory (one atomic per non-empty bin) when the CTA
-// leaves a group.
+// flushed to global memory when the CTA leaves a group -- from the top bin
+// down to where this CTA alone holds min(K, L) keys, which keeps the global
+// histogram exact from the Top-K threshold digit up (flush_hist).
 #include <cuda.h>
 
 #include <algorithm>
@@ -51,7 +52,7 @@ struct ScanArgs {
     float *scores;
     uint32_t *hist;
     uint32_t *status;
-    int B, Hq, Hkv, G, max_len, sc_stride, len_off, stages;
+    int B, Hq, Hkv, G, max_len, sc_stride, len_off, stages, K;
     float scale;
 };
 
@@ -86,7 +87,7 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint3
 // Adds the shared-memory histograms of the exact heads in `mask` (G heads of
 // kHistBins bins) into global memory: 16-byte shared loads, one atomic per
 // non-empty bin.  Called by the 256 consumer threads.
-__device__ __forceinline__ void flush_hist(const uint32_t *hist_s, uint32_t *hg, int G, uint32_t mask, int tid)
+__device__ __forceinline__ void flush_hist_all(const uint32_t *hist_s, uint32_t *hg, int G, uint32_t mask, int tid)
 {
     constexpr int kVec = kHistBins / 4;
     for (int i4 = tid; i4 < G * kVec; i4 += 256) {
@@ -103,6 +104,53 @@ __device__ __forceinline__ void flush_hist(const uint32_t *hist_s, uint32_t *hg,
         if (h.w)
             atomicAdd(d + 3, h.w);
     }
+}
+
+// The same, when the CTA holds many keys of many exact heads: only the top of
+// a histogram is used -- the select takes from it the digit T1 of the
+// need-th largest score, and the bins from T1 up must be complete.  If this
+// CTA alone holds `need` keys at or above digit th, the global T1 is >= th;
+// so each CTA flushing its bins from the top down to its own th keeps every
+// bin >= T1 exact.  Consumer warp w takes heads w, w + 8, ...: 128 bins per
+// step from the top (lane 0 the highest four), one atomic per nonzero bin,
+// until the step in which its running count reaches need.  Fewer atomics than
+// flush_hist_all when each head holds several times `need` keys here (one
+// warp per head is slower when only one or two heads are exact).
+__device__ __forceinline__ void flush_hist_top(const uint32_t *hist_s, uint32_t *hg, int G, uint32_t mask, int need,
+                                               int tid)
+{
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int n = warp; n < G; n += kConsumerWarps) {
+        if (!((mask >> n) & 1u))
+            continue;
+        const uint32_t *hs = hist_s + (size_t)n * kHistBins;
+        uint32_t *hd = hg + (size_t)n * kHistBins;
+        int run = 0;
+        for (int top = kHistBins; top > 0 && run < need; top -= 128) {   // warp-uniform
+            const int base = top - 4 * (lane + 1);
+            const uint4 h = *reinterpret_cast<const uint4 *>(hs + base);
+            if (h.x)
+                atomicAdd(hd + base, h.x);
+            if (h.y)
+                atomicAdd(hd + base + 1, h.y);
+            if (h.z)
+                atomicAdd(hd + base + 2, h.z);
+            if (h.w)
+                atomicAdd(hd + base + 3, h.w);
+            run += warp_isum((int)(h.x + h.y + h.z + h.w));
+        }
+    }
+}
+
+// The group's histograms into global memory: the top-only flush when this CTA
+// scored at least 4 * need rows of the group for at least four exact heads.
+__device__ __forceinline__ void flush_hist(const uint32_t *hist_s, uint32_t *hg, int G, uint32_t mask, int need,
+                                           int rows, int tid)
+{
+    if (rows >= 4 * need && __popc(mask) >= 4)
+        flush_hist_top(hist_s, hg, G, mask, need, tid);
+    else
+        flush_hist_all(hist_s, hg, G, mask, tid);
 }
 
 __device__ __forceinline__ void consumer_sync()
@@ -147,7 +195,14 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    pdl_wait();      // the path decision
+    // Without a path decision (the stateless exact step, cache initialisation)
+    // nothing the tiles or the tile list read comes from the previous kernel
+    // (the histogram clear, itself a plain launch behind everything earlier):
+    // the copies start at once and only the histogram flush waits for it.
+    // A decode step's scan needs the decision (and the appended K row) first.
+    const bool early = a.path == nullptr;
+    if (!early)
+        pdl_wait();
     pdl_trigger();
     // ---- active groups and their tile ranges (every CTA computes the same
     //      list): groups with no exact head get zero tiles
@@ -222,6 +277,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         uint64_t keep;
         asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
         int gi = -1;
+        int grp_rows = 0;   // rows of the current group this CTA has scored (flush heuristic)
         uint32_t mask = 0;
         int b = 0, hk = 0, L = 0;
         uint4 qf[NT][4];
@@ -234,10 +290,14 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             if (ng != gi) {
                 consumer_sync();
                 if (gi >= 0) {   // flush the previous group's histogram
-                    flush_hist(hist_s, a.hist + (size_t)(b * a.Hq + hk * G) * kHistBins, G, mask, tid);
+                    if (early)
+                        pdl_wait();   // the histograms are cleared
+                    flush_hist(hist_s, a.hist + (size_t)(b * a.Hq + hk * G) * kHistBins, G, mask, min(a.K, L),
+                               grp_rows, tid);
                     consumer_sync();
                 }
                 gi = ng;
+                grp_rows = 0;
                 mask = sh.grp_mask[gi];
                 b = gi / a.Hkv;
                 hk = gi % a.Hkv;
@@ -268,6 +328,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 continue;   // keep walking the tiles so the named barriers still match
             const unsigned char *st = ring + (size_t)s * kStageBytes;
             const int base = (tile - sh.grp_first[gi]) * kTileRows;   // first row of the tile
+            grp_rows += kTileRows;
             const int rl0 = warp * 16 + row_perm(g), rl1 = rl0 + 8;    // rows within the tile
             uint4 x0[4], x1[4];
 #pragma unroll
@@ -314,8 +375,11 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             }
         }
         consumer_sync();
+        if (early)
+            pdl_wait();   // the histograms are cleared
         if (gi >= 0)
-            flush_hist(hist_s, a.hist + (size_t)(b * a.Hq + hk * G) * kHistBins, G, mask, tid);
+            flush_hist(hist_s, a.hist + (size_t)(b * a.Hq + hk * G) * kHistBins, G, mask, min(a.K, L), grp_rows,
+                       tid);
         if (nonfinite)
             atomicOr(a.status, RETOPK_STATUS_NONFINITE);
     }
@@ -426,6 +490,7 @@ cudaError_t launch_scan(const Work &w, QSrc q, const uint16_t *k_cache, const in
     a.max_len = w.max_len;
     a.sc_stride = w.sc_stride;
     a.len_off = len_off;
+    a.K = w.K;
     a.stages = std::max(2, std::min(stages_for(w.G), max_stages));
     a.scale = 1.0f / sqrtf((float)kD);
     const size_t smem = 1024 + (size_t)a.stages * kStageBytes + hist_bytes(w.G);

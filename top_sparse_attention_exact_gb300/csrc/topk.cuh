@@ -172,7 +172,8 @@ __device__ unsigned long long radix_select_threshold(int N, int need, Get get, S
 // candidates of each NT*E chunk, so one block scan covers the chunk.  The
 // outputs may alias the candidate arrays read by `get` (positions written never
 // exceed the position read, and every read of a chunk precedes its writes).
-// Returns the count.
+// Returns the count.  The last chunk's writes are not followed by a barrier:
+// synchronise the block before other threads read the outputs.
 template <int NT, int E = 8, class Get>
 __device__ int stable_compact(int N, unsigned long long thr, Get get, int cap, int32_t *out_i,
                               uint32_t *out_k, int *warp_tot)
