@@ -110,6 +110,28 @@ size_t retopk_workspace_bytes(const retopk_config *cfg);
 int retopk_create(const retopk_config *cfg, void *d_workspace, size_t bytes, retopk_ctx **out);
 int retopk_destroy(retopk_ctx *ctx);
 
+/* The same context with its device memory in two parts, so that several
+ * contexts -- the layers of a model, each with its own configuration of the
+ * same sizes and its own caches -- can share the larger one.
+ *   state   (>= retopk_state_workspace_bytes, 256-byte aligned): the context's
+ *           own query-support cache (Eq. (5)), ring words, counters and status
+ *           word; cleared here.
+ *   scratch (>= retopk_scratch_bytes, 256-byte aligned): what a decode step
+ *           writes and reads within the step (path decisions, candidate lists,
+ *           scores, histograms) and the last step's diagnostics.  Contexts may
+ *           share one scratch when their calls never overlap on the GPU: calls
+ *           on one stream one after another (captured into one graph or not) are
+ *           fine, calls on concurrent streams are not.  retopk_get_diagnostics
+ *           and retopk_fidelity report the last step run with the scratch, by
+ *           whichever context.
+ * (The ReTopK paper's fused implementation likewise reuses per-layer
+ * workspaces, §Experiments Table 4.)  Synchronises the current device once.
+ * Both buffers must outlive the context. */
+size_t retopk_state_workspace_bytes(const retopk_config *cfg);
+size_t retopk_scratch_bytes(const retopk_config *cfg);
+int retopk_create_shared(const retopk_config *cfg, void *d_state, size_t state_bytes, void *d_scratch,
+                         size_t scratch_bytes, retopk_ctx **out);
+
 /* ---- ReTopK decode ------------------------------------------------------ */
 
 /* Cache initialisation from the final C prompt tokens (§Recall-Before-Rerank,
@@ -244,6 +266,27 @@ int exact_topk_attention_step(const retopk_bf16 *q, const retopk_bf16 *k_cache,
                               int B, int Hq, int Hkv, int d, int max_len, int K,
                               retopk_bf16 *out, int32_t *idx_out,
                               void *d_workspace, size_t bytes, void *stream);
+
+/* The two halves of exact_topk_attention_step, for callers that place other
+ * work between them or time them apart; run back to back on one stream with
+ * the same workspace (and the same q, seqlens and sizes) they give the same
+ * results as exact_topk_attention_step.
+ *   exact_topk_scan:   §Problem Setup Eq. (4), e_i = q.k_i / sqrt(d) for every
+ *                      key of every (b, h), left in the workspace together with
+ *                      the histogram of their first radix digit (the
+ *                      workspace's histograms are cleared first).
+ *   exact_topk_select: §Motivation Eq. (1), the K best of those scores (ties
+ *                      to the lower index), then §Recall-Before-Rerank
+ *                      Eq. (12) over them; out / idx_out as for
+ *                      exact_topk_attention_step.
+ * The select half must follow a scan half with the same workspace; anything
+ * else that writes the workspace in between invalidates it.  Both are
+ * asynchronous on `stream` and graph-capturable. */
+int exact_topk_scan(const retopk_bf16 *q, const retopk_bf16 *k_cache, const int32_t *d_seqlens, int B, int Hq,
+                    int Hkv, int d, int max_len, int K, void *d_workspace, size_t bytes, void *stream);
+int exact_topk_select(const retopk_bf16 *q, const retopk_bf16 *v_cache, const int32_t *d_seqlens, int B, int Hq,
+                      int Hkv, int d, int max_len, int K, retopk_bf16 *out, int32_t *idx_out, void *d_workspace,
+                      size_t bytes, void *stream);
 
 /* Allocation-free variant of exact_topk_attention_step (the paper has no
  * counterpart; it exists for callers that cannot allocate device memory at

@@ -447,6 +447,53 @@ def test_fused_append_matches_separate_calls():
         assert torch.equal(a.k_cache, x.k_cache) and torch.equal(a.v_cache, x.v_cache)
 
 
+def test_layer_stack_shared_scratch_matches_per_layer_steps():
+    # several layer contexts (own caches, own query-support state) sharing one
+    # per-step scratch, stepped as one captured graph per token with the layers
+    # back to back, against each layer stepped eagerly with its own full
+    # workspace: identical outputs every step and identical final states
+    from top_sparse_attention_exact_gb300 import retopk
+    w0 = synth.scaled(synth.WORKLOADS["qwen7b_16k"], L0=4096, steps=24, T_r=8, name="stack")
+    n_layers = 4
+    ws = [synth.scaled(w0, seeds=(50 + i,)) for i in range(n_layers)]
+    arrays = [synth.generate(w) for w in ws]
+    nb = retopk.scratch_bytes(w0.B, w0.Hq, w0.Hkv, w0.max_len, w0.K, w0.C, w0.W, w0.R, w0.T_r, w0.tau)
+    scratch = torch.empty(nb + 256, dtype=torch.uint8, device="cuda")
+    stack = [DecodeRun(w, arrays=a, scratch=scratch) for w, a in zip(ws, arrays)]
+    ref = [DecodeRun(w, arrays=a) for w, a in zip(ws, arrays)]
+    bufs = [(torch.empty_like(r.q_dec[0]), torch.empty_like(r.k_new[0]), torch.empty_like(r.v_new[0])) for r in stack]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for r, (qb, kb, vb) in zip(stack, bufs):
+                r.ctx.retopk_decode_step_kv(kb, vb, qb, r.k_cache, r.v_cache, r.seqlens, r.out, s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    paths = []
+    for t in range(w0.steps):
+        for r, (qb, kb, vb) in zip(stack, bufs):
+            qb.copy_(r.q_dec[t])
+            kb.copy_(r.k_new[t])
+            vb.copy_(r.v_new[t])
+        g.replay()
+        for r in ref:
+            r.step(t)
+            paths.append(r.ctx.retopk_get_diagnostics()["path"].copy())
+        torch.cuda.synchronize()
+        for i in range(n_layers):
+            assert torch.equal(stack[i].out, ref[i].out), (t, i)
+    for i in range(n_layers):
+        sa, sb = stack[i].ctx.retopk_export_state(), ref[i].ctx.retopk_export_state()
+        for key in sa:
+            assert np.array_equal(sa[key], sb[key]), (i, key)
+        assert torch.equal(stack[i].k_cache, ref[i].k_cache) and torch.equal(stack[i].seqlens, ref[i].seqlens)
+        assert stack[i].ctx.retopk_get_status() == 0
+    p = np.concatenate(paths)
+    assert (p == 0).sum() > 0 and (p != 0).sum() > 0   # both paths were exercised
+
+
 def test_state_round_trip_and_status_bits():
     # tau = -1 with no refresh: every head reuses, so every head reads the
     # corrupted cached supports below

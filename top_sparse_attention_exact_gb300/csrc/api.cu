@@ -129,8 +129,88 @@ int cand_stride_for(int max_len, int RKW)
     return (s + 63) & ~63;
 }
 
-// Fills the sizes (and, when base != NULL, the pointers) of a workspace.
-size_t plan(const retopk_config &c, bool stateful, Work *w, char *base)
+// The per-context state of a decode context: the query-support cache of
+// Eq. (5), the ring words, the counters and the sticky status word.  Fills the
+// pointers when base != NULL; returns the bytes.
+size_t plan_state(const retopk_config &c, Work *w, char *base)
+{
+    const size_t BH = (size_t)c.batch * c.n_q_heads;
+    Layout L;
+    const size_t o_fq = L.add(BH * c.C * kD * 2);
+    const size_t o_fs = L.add(BH * c.C * c.K * 4);
+    const size_t o_fl = L.add(BH * c.C * 4);
+    const size_t o_seq = L.add((size_t)c.batch * SEQ_WORDS * 4);
+    const size_t o_cnt = L.add((size_t)c.batch * CNT_WORDS * 8);
+    const size_t o_st = L.add(16);
+    if (base && w) {
+        w->fifo_q = (uint16_t *)(base + o_fq);
+        w->fifo_sup = (int32_t *)(base + o_fs);
+        w->fifo_len = (int32_t *)(base + o_fl);
+        w->seq = (int32_t *)(base + o_seq);
+        w->counters = (unsigned long long *)(base + o_cnt);
+        w->status = (uint32_t *)(base + o_st);
+    }
+    return L.total + kAlign;
+}
+
+// The per-step scratch: written and read within one step (plus the last
+// step's diagnostics), so the steps of several contexts that never overlap on
+// the GPU can share it.  `stateful` adds the decode-only buffers; a stateless
+// exact step also keeps its status word here.  Fills the sizes (and, when
+// base != NULL, the pointers); returns the bytes.
+size_t plan_scratch(const retopk_config &c, bool stateful, Work *w, char *base)
+{
+    const int RKW = stateful ? c.R * c.K + c.W : 0;
+    const int cand_stride = cand_stride_for(c.max_len, RKW);
+    const int sc_stride = (c.max_len + 15) & ~15;
+    const size_t BH = (size_t)c.batch * c.n_q_heads;
+    Layout L;
+    size_t o_snap = 0, o_path = 0, o_rho = 0, o_topr = 0, o_qs = 0, o_st = 0;
+    if (stateful) {
+        o_snap = L.add((size_t)c.batch * SEQ_WORDS * 4);
+        o_path = L.add(BH * 4);
+        o_rho = L.add(BH * 4);
+        o_topr = L.add(BH * c.R * 4);
+        o_qs = L.add(BH * kD * 2);
+    } else {
+        o_st = L.add(16);
+    }
+    const size_t o_M = L.add(BH * 4);
+    const size_t o_ci = L.add(BH * cand_stride * 4);
+    const size_t o_ck = L.add(BH * cand_stride * 4);
+    const size_t o_sc = L.add(BH * (size_t)sc_stride * 4);
+    const size_t o_h = L.add(BH * kHistBins * 4);
+    const size_t o_sup = L.add(BH * c.K * 4);
+    const size_t o_sl = L.add(BH * 4);
+    const size_t o_of = L.add(BH * kD * 4);
+    if (w) {
+        w->cand_stride = cand_stride;
+        w->sc_stride = sc_stride;
+    }
+    if (base && w) {
+        if (stateful) {
+            w->snap = (int32_t *)(base + o_snap);
+            w->path = (int32_t *)(base + o_path);
+            w->rho_max = (float *)(base + o_rho);
+            w->topR = (int32_t *)(base + o_topr);
+            w->q_stage = (uint16_t *)(base + o_qs);
+        } else {
+            w->status = (uint32_t *)(base + o_st);
+        }
+        w->M = (int32_t *)(base + o_M);
+        w->cand_idx = (int32_t *)(base + o_ci);
+        w->cand_key = (uint32_t *)(base + o_ck);
+        w->scores = (float *)(base + o_sc);
+        w->hist = (uint32_t *)(base + o_h);
+        w->support = (int32_t *)(base + o_sup);
+        w->sup_len = (int32_t *)(base + o_sl);
+        w->out_f32 = (float *)(base + o_of);
+    }
+    return L.total + kAlign;
+}
+
+// The configuration's scalar fields in a Work (no buffers).
+Work work_of(const retopk_config &c)
 {
     Work x;
     memset(&x, 0, sizeof x);
@@ -146,60 +226,20 @@ size_t plan(const retopk_config &c, bool stateful, Work *w, char *base)
     x.T_r = c.T_r;
     x.tau = c.tau;
     x.retrieval = c.retrieval;
-    const int RKW = stateful ? c.R * c.K + c.W : 0;
-    x.cand_stride = cand_stride_for(c.max_len, RKW);
-    x.sc_stride = (c.max_len + 15) & ~15;
-    const size_t BH = (size_t)c.batch * c.n_q_heads;
-    Layout L;
-    size_t o_fq = 0, o_fs = 0, o_fl = 0, o_seq = 0, o_snap = 0, o_cnt = 0, o_path = 0, o_rho = 0, o_topr = 0,
-           o_qs = 0;
-    if (stateful) {
-        o_fq = L.add(BH * c.C * kD * 2);
-        o_fs = L.add(BH * c.C * c.K * 4);
-        o_fl = L.add(BH * c.C * 4);
-        o_seq = L.add((size_t)c.batch * SEQ_WORDS * 4);
-        o_snap = L.add((size_t)c.batch * SEQ_WORDS * 4);
-        o_cnt = L.add((size_t)c.batch * CNT_WORDS * 8);
-        o_path = L.add(BH * 4);
-        o_rho = L.add(BH * 4);
-        o_topr = L.add(BH * c.R * 4);
-        o_qs = L.add(BH * kD * 2);
-    }
-    const size_t o_M = L.add(BH * 4);
-    const size_t o_ci = L.add(BH * x.cand_stride * 4);
-    const size_t o_ck = L.add(BH * x.cand_stride * 4);
-    const size_t o_sc = L.add(BH * (size_t)x.sc_stride * 4);
-    const size_t o_h = L.add(BH * kHistBins * 4);
-    const size_t o_sup = L.add(BH * c.K * 4);
-    const size_t o_sl = L.add(BH * 4);
-    const size_t o_of = L.add(BH * kD * 4);
-    const size_t o_st = L.add(16);
-    if (base) {
-        if (stateful) {
-            x.fifo_q = (uint16_t *)(base + o_fq);
-            x.fifo_sup = (int32_t *)(base + o_fs);
-            x.fifo_len = (int32_t *)(base + o_fl);
-            x.seq = (int32_t *)(base + o_seq);
-            x.snap = (int32_t *)(base + o_snap);
-            x.counters = (unsigned long long *)(base + o_cnt);
-            x.path = (int32_t *)(base + o_path);
-            x.rho_max = (float *)(base + o_rho);
-            x.topR = (int32_t *)(base + o_topr);
-            x.q_stage = (uint16_t *)(base + o_qs);
-        }
-        x.M = (int32_t *)(base + o_M);
-        x.cand_idx = (int32_t *)(base + o_ci);
-        x.cand_key = (uint32_t *)(base + o_ck);
-        x.scores = (float *)(base + o_sc);
-        x.hist = (uint32_t *)(base + o_h);
-        x.support = (int32_t *)(base + o_sup);
-        x.sup_len = (int32_t *)(base + o_sl);
-        x.out_f32 = (float *)(base + o_of);
-        x.status = (uint32_t *)(base + o_st);
-    }
+    return x;
+}
+
+// One workspace holding everything: a decode context's state then its
+// scratch, or a stateless exact step's scratch.  Fills the pointers when
+// base != NULL; returns the bytes.
+size_t plan(const retopk_config &c, bool stateful, Work *w, char *base)
+{
+    Work x = work_of(c);
+    const size_t ns = stateful ? plan_state(c, &x, base) : 0;
+    const size_t nt = plan_scratch(c, stateful, &x, base ? base + ns : nullptr);
     if (w)
         *w = x;
-    return L.total + kAlign;
+    return ns + nt;
 }
 
 int check_dims(int B, int Hq, int Hkv, int d, int max_len, int K)
@@ -341,6 +381,57 @@ size_t retopk_workspace_bytes(const retopk_config *cfg)
     if (check_cfg(cfg))
         return 0;
     return plan(*cfg, true, nullptr, nullptr);
+}
+
+size_t retopk_state_workspace_bytes(const retopk_config *cfg)
+{
+    if (check_cfg(cfg))
+        return 0;
+    return plan_state(*cfg, nullptr, nullptr);
+}
+
+size_t retopk_scratch_bytes(const retopk_config *cfg)
+{
+    if (check_cfg(cfg))
+        return 0;
+    return plan_scratch(*cfg, true, nullptr, nullptr);
+}
+
+int retopk_create_shared(const retopk_config *cfg, void *d_state, size_t state_bytes, void *d_scratch,
+                         size_t scratch_bytes, retopk_ctx **out)
+{
+    int e = check_cfg(cfg);
+    if (e)
+        return e;
+    if (!out || !d_state || !d_scratch)
+        return RETOPK_ERR_INVALID;
+    const size_t ns = plan_state(*cfg, nullptr, nullptr), nt = plan_scratch(*cfg, true, nullptr, nullptr);
+    if (((uintptr_t)d_state & (kAlign - 1)) != 0 || ((uintptr_t)d_scratch & (kAlign - 1)) != 0 ||
+        state_bytes < ns || scratch_bytes < nt)
+        return RETOPK_ERR_WORKSPACE;
+    if ((e = ensure_configured()))
+        return e;
+    retopk_ctx *c = (retopk_ctx *)calloc(1, sizeof(retopk_ctx));
+    if (!c)
+        return RETOPK_ERR_INVALID;
+    c->cfg = *cfg;
+    c->ws = d_state;
+    c->ws_bytes = state_bytes;
+    cudaGetDevice(&c->device);
+    c->w = work_of(*cfg);
+    plan_state(*cfg, &c->w, (char *)d_state);
+    plan_scratch(*cfg, true, &c->w, (char *)d_scratch);
+    c->w.n_scan = n_scan_for(cfg->batch, cfg->n_kv_heads, cfg->max_len);
+    // the state starts at zero; the scratch holds nothing a step reads before writing it
+    cudaError_t ce = cudaMemset(d_state, 0, ns);
+    if (ce == cudaSuccess)
+        ce = cudaDeviceSynchronize();
+    if (ce != cudaSuccess) {
+        free(c);
+        return cuda_rc(ce);
+    }
+    *out = c;
+    return RETOPK_OK;
 }
 
 int retopk_create(const retopk_config *cfg, void *d_workspace, size_t bytes, retopk_ctx **out)
@@ -793,6 +884,58 @@ size_t exact_topk_workspace_bytes(int B, int Hq, int Hkv, int d, int max_len, in
     return plan(c, false, nullptr, nullptr);
 }
 
+}  // extern "C"
+
+namespace {
+
+// The device view of a stateless exact step's workspace (both halves use it).
+int exact_work(int B, int Hq, int Hkv, int d, int max_len, int K, void *d_workspace, size_t bytes, Work *w)
+{
+    int e = check_dims(B, Hq, Hkv, d, max_len, K);
+    if (e)
+        return e;
+    if (!d_workspace)
+        return RETOPK_ERR_INVALID;
+    retopk_config c{B, Hq, Hkv, d, max_len, K, 1, 0, 1, 0, 0.f};
+    const size_t need = plan(c, false, nullptr, nullptr);
+    if (((uintptr_t)d_workspace & (kAlign - 1)) != 0 || bytes < need)
+        return RETOPK_ERR_WORKSPACE;
+    if ((e = ensure_configured()))
+        return e;
+    plan(c, false, w, (char *)d_workspace);
+    w->n_scan = n_scan_for(B, Hkv, max_len);
+    w->out_f32 = nullptr;
+    w->support = nullptr;
+    return RETOPK_OK;
+}
+
+// Eq. (4) for every key of every (b, h) into the workspace's scores, with the
+// first radix digit's histograms (cleared first).
+int exact_scan_half(const Work &w, const retopk_bf16 *q, const retopk_bf16 *k_cache, const int32_t *d_seqlens,
+                    cudaStream_t st)
+{
+    int e;
+    if ((e = cuda_rc(timed(RETOPK_PROF_CLEAR, st, [&] {
+             return launch_clear_words(w.hist, (size_t)w.B * w.Hq * kHistBins * 4, st);
+         }))))
+        return e;
+    return run_scan(w, QSrc{q, (long long)w.Hq * kD, kD}, k_cache, d_seqlens, 0, st);
+}
+
+// Eq. (1) over the scores the scan half left in the workspace, then Eq. (12).
+int exact_select_half(const Work &w, const retopk_bf16 *q, const retopk_bf16 *v_cache, const int32_t *d_seqlens,
+                      retopk_bf16 *out, int32_t *idx_out, cudaStream_t st)
+{
+    return cuda_rc(timed(RETOPK_PROF_SELECT, st, [&] {
+        return launch_exact_select(w, QSrc{q, (long long)w.Hq * kD, kD}, v_cache, d_seqlens, 0, FIN_EXACT, 0, out,
+                                   idx_out, st);
+    }));
+}
+
+}  // namespace
+
+extern "C" {
+
 int exact_topk_attention_step(const retopk_bf16 *q, const retopk_bf16 *k_cache, const retopk_bf16 *v_cache,
                               const int32_t *d_seqlens, int B, int Hq, int Hkv, int d, int max_len, int K,
                               retopk_bf16 *out, int32_t *idx_out, void *d_workspace, size_t bytes,
@@ -805,27 +948,46 @@ int exact_topk_attention_step(const retopk_bf16 *q, const retopk_bf16 *k_cache, 
         return RETOPK_ERR_INVALID;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
         return RETOPK_ERR_ALIGN;
-    retopk_config c{B, Hq, Hkv, d, max_len, K, 1, 0, 1, 0, 0.f};
-    const size_t need = plan(c, false, nullptr, nullptr);
-    if (((uintptr_t)d_workspace & (kAlign - 1)) != 0 || bytes < need)
-        return RETOPK_ERR_WORKSPACE;
-    if ((e = ensure_configured()))
-        return e;
     Work w;
-    plan(c, false, &w, (char *)d_workspace);
-    w.n_scan = n_scan_for(B, Hkv, max_len);
-    w.out_f32 = nullptr;
-    w.support = nullptr;
+    if ((e = exact_work(B, Hq, Hkv, d, max_len, K, d_workspace, bytes, &w)))
+        return e;
     cudaStream_t st = (cudaStream_t)stream;
-    QSrc qs{q, (long long)Hq * kD, kD};
-    if ((e = cuda_rc(timed(RETOPK_PROF_CLEAR, st,
-                           [&] { return launch_clear_words(w.hist, (size_t)B * Hq * kHistBins * 4, st); }))))
+    if ((e = exact_scan_half(w, q, k_cache, d_seqlens, st)))
         return e;
-    if ((e = run_scan(w, qs, k_cache, d_seqlens, 0, st)))
+    return exact_select_half(w, q, v_cache, d_seqlens, out, idx_out, st);
+}
+
+int exact_topk_scan(const retopk_bf16 *q, const retopk_bf16 *k_cache, const int32_t *d_seqlens, int B, int Hq,
+                    int Hkv, int d, int max_len, int K, void *d_workspace, size_t bytes, void *stream)
+{
+    int e = check_dims(B, Hq, Hkv, d, max_len, K);
+    if (e)
         return e;
-    return cuda_rc(timed(RETOPK_PROF_SELECT, st, [&] {
-        return launch_exact_select(w, qs, v_cache, d_seqlens, 0, FIN_EXACT, 0, out, idx_out, st);
-    }));
+    if (!q || !k_cache || !d_seqlens || !d_workspace)
+        return RETOPK_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k_cache))
+        return RETOPK_ERR_ALIGN;
+    Work w;
+    if ((e = exact_work(B, Hq, Hkv, d, max_len, K, d_workspace, bytes, &w)))
+        return e;
+    return exact_scan_half(w, q, k_cache, d_seqlens, (cudaStream_t)stream);
+}
+
+int exact_topk_select(const retopk_bf16 *q, const retopk_bf16 *v_cache, const int32_t *d_seqlens, int B, int Hq,
+                      int Hkv, int d, int max_len, int K, retopk_bf16 *out, int32_t *idx_out, void *d_workspace,
+                      size_t bytes, void *stream)
+{
+    int e = check_dims(B, Hq, Hkv, d, max_len, K);
+    if (e)
+        return e;
+    if (!q || !v_cache || !d_seqlens || !out || !d_workspace)
+        return RETOPK_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(v_cache) || !aligned16(out))
+        return RETOPK_ERR_ALIGN;
+    Work w;
+    if ((e = exact_work(B, Hq, Hkv, d, max_len, K, d_workspace, bytes, &w)))
+        return e;
+    return exact_select_half(w, q, v_cache, d_seqlens, out, idx_out, (cudaStream_t)stream);
 }
 
 // ---- allocation-free Exact Top-K step ---------------------------------------

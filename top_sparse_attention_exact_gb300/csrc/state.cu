@@ -56,10 +56,14 @@ __global__ void init_done_kernel(int32_t *seq, unsigned long long *counters, int
     }
 }
 
-// Zeroes n4 uint4 words (the exact step's histograms); lets the scan that
-// follows start its set-up at once (it waits for this grid before its flush).
+// Zeroes n4 uint4 words (the exact step's histograms).  Launched
+// programmatically, so its CTAs may become resident while the previous kernel
+// drains; it waits for that kernel (which may still read the words) before it
+// writes, then lets the scan that follows start (the scan reads nothing this
+// kernel writes before its own wait for this grid, ahead of its flush).
 __global__ void clear_words_kernel(uint4 *p, long long n4)
 {
+    pdl_wait();
     pdl_trigger();
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x)
         p[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -69,8 +73,8 @@ cudaError_t launch_clear_words(void *p, size_t bytes, cudaStream_t st)
 {
     const long long n4 = (long long)(bytes / 16);
     const int blocks = (int)std::min<long long>(152, (n4 + 255) / 256);
-    clear_words_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(reinterpret_cast<uint4 *>(p), n4);
-    return cudaGetLastError();
+    return launch_pdl(clear_words_kernel, dim3(blocks > 0 ? blocks : 1), dim3(256), 0, st, 1,
+                      reinterpret_cast<uint4 *>(p), n4);
 }
 
 cudaError_t launch_init_done(const Work &w, cudaStream_t st)

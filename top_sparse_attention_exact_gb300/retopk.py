@@ -28,7 +28,8 @@ EXPORTED = ("retopk_workspace_bytes", "retopk_create", "retopk_destroy", "retopk
             "exact_topk_workspace_bytes", "exact_topk_attention_step",
             "retopk_profile_enable", "retopk_profile_read", "retopk_profile_reset",
             "retopk_selftest_wait", "exact_topk_attention_step_noalloc", "retopk_fidelity",
-            "retopk_decode_step_host", "retopk_support_overlap")
+            "retopk_decode_step_host", "retopk_support_overlap", "exact_topk_scan", "exact_topk_select",
+            "retopk_state_workspace_bytes", "retopk_scratch_bytes", "retopk_create_shared")
 
 PROF_KERNELS = ("append", "finish", "scan", "select", "clear", "decide")
 
@@ -54,6 +55,11 @@ def _declare(lib):
     lib.retopk_workspace_bytes.restype = _S
     lib.retopk_create.argtypes = [cfgp, _P, _S, ctypes.POINTER(_P)]
     lib.retopk_destroy.argtypes = [_P]
+    lib.retopk_state_workspace_bytes.argtypes = [cfgp]
+    lib.retopk_state_workspace_bytes.restype = _S
+    lib.retopk_scratch_bytes.argtypes = [cfgp]
+    lib.retopk_scratch_bytes.restype = _S
+    lib.retopk_create_shared.argtypes = [cfgp, _P, _S, _P, _S, ctypes.POINTER(_P)]
     lib.retopk_init_cache.argtypes = [_P, _P, _P, _P, _P]
     lib.retopk_append_kv.argtypes = [_P, _P, _P, _P, _P, _P, _P]
     lib.retopk_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P]
@@ -80,6 +86,8 @@ def _declare(lib):
     lib.retopk_selftest_wait.argtypes = [_P, ctypes.c_int64, _P]
     lib.exact_topk_attention_step_noalloc.argtypes = [_P, _P, _P, _P] + [_I] * 6 + [_P, _P, _P]
     lib.retopk_support_overlap.argtypes = [_P, _P, _I, _I, _I, _P, _P]
+    lib.exact_topk_scan.argtypes = [_P, _P, _P] + [_I] * 6 + [_P, _S, _P]
+    lib.exact_topk_select.argtypes = [_P, _P, _P] + [_I] * 6 + [_P, _P, _P, _S, _P]
     for name in EXPORTED:
         getattr(lib, name).restype = getattr(lib, name).restype or ctypes.c_int
     return lib
@@ -172,6 +180,35 @@ def exact_topk_attention_step(q, k_cache, v_cache, seqlens, K, out, idx_out=None
     return out
 
 
+def _exact_ws(workspace, B, Hq, Hkv, d, max_len, K, device):
+    if workspace is None:
+        workspace = torch.empty(exact_topk_workspace_bytes(B, Hq, Hkv, d, max_len, K) + 256, dtype=torch.uint8,
+                                device=device)
+    wp = (workspace.data_ptr() + 255) // 256 * 256
+    return workspace, wp, workspace.numel() - (wp - workspace.data_ptr())
+
+
+def exact_topk_scan(q, k_cache, seqlens, K, workspace, stream=None):
+    """First half of the exact step: Eq. (4) scores and first-digit histograms into `workspace`."""
+    B, Hq, d = q.shape
+    Hkv, max_len = k_cache.shape[1], k_cache.shape[2]
+    workspace, wp, avail = _exact_ws(workspace, B, Hq, Hkv, d, max_len, K, q.device)
+    _check(load().exact_topk_scan(_ptr(_bf16(q)), _ptr(_bf16(k_cache)), _ptr(_i32(seqlens)), B, Hq, Hkv, d, max_len,
+                                  int(K), ctypes.c_void_p(wp), avail, _stream(stream)), "exact_topk_scan")
+    return workspace
+
+
+def exact_topk_select(q, v_cache, seqlens, K, out, idx_out, workspace, stream=None):
+    """Second half of the exact step: Eq. (1) and Eq. (12) from the scan half's workspace."""
+    B, Hq, d = q.shape
+    Hkv, max_len = v_cache.shape[1], v_cache.shape[2]
+    workspace, wp, avail = _exact_ws(workspace, B, Hq, Hkv, d, max_len, K, q.device)
+    _check(load().exact_topk_select(_ptr(_bf16(q)), _ptr(_bf16(v_cache)), _ptr(_i32(seqlens)), B, Hq, Hkv, d,
+                                    max_len, int(K), _ptr(_bf16(out)), _ptr(idx_out) if idx_out is not None else None,
+                                    ctypes.c_void_p(wp), avail, _stream(stream)), "exact_topk_select")
+    return out
+
+
 def exact_topk_attention_step_noalloc(q, k_cache, v_cache, seqlens, K, out, idx_out=None, stream=None):
     """Exact Top-K attention with the library's static scratch (no workspace)."""
     B, Hq, d = q.shape
@@ -197,6 +234,15 @@ def support_overlap(S, others, stream=None):
     return out
 
 
+def scratch_bytes(B, Hq, Hkv, max_len, K=512, C=32, W=32, R=4, T_r=128, tau=0.85, d=128, recent=False) -> int:
+    """Bytes of the per-step scratch a context of this configuration needs (retopk_scratch_bytes)."""
+    cfg = retopk_config(B, Hq, Hkv, d, max_len, K, C, W, R, T_r, tau, 1 if recent else 0)
+    n = load().retopk_scratch_bytes(ctypes.byref(cfg))
+    if n == 0:
+        raise RetopkError("retopk_scratch_bytes: invalid configuration")
+    return int(n)
+
+
 def profile_enable(on: bool):
     _check(load().retopk_profile_enable(1 if on else 0), "retopk_profile_enable")
 
@@ -218,17 +264,31 @@ class ReTopK:
     """A ReTopK decode context (query-support cache + scratch in a torch buffer)."""
 
     def __init__(self, B, Hq, Hkv, max_len, K=512, C=32, W=32, R=4, T_r=128, tau=0.85, d=128,
-                 device="cuda", recent: bool = False):
+                 device="cuda", recent: bool = False, scratch: torch.Tensor | None = None):
+        """scratch: optional uint8 CUDA tensor of at least scratch_bytes(...) + 256 bytes, shared with
+        other contexts whose steps run one after another on one stream (retopk_create_shared)."""
         self.cfg = retopk_config(B, Hq, Hkv, d, max_len, K, C, W, R, T_r, tau, 1 if recent else 0)
         lib = load()
-        n = lib.retopk_workspace_bytes(ctypes.byref(self.cfg))
-        if n == 0:
-            raise RetopkError("retopk_workspace_bytes: invalid configuration")
-        self.workspace = torch.empty(int(n) + 256, dtype=torch.uint8, device=device)
-        wp = (self.workspace.data_ptr() + 255) // 256 * 256
         h = ctypes.c_void_p()
-        _check(lib.retopk_create(ctypes.byref(self.cfg), ctypes.c_void_p(wp), int(n), ctypes.byref(h)),
-               "retopk_create")
+        if scratch is None:
+            n = lib.retopk_workspace_bytes(ctypes.byref(self.cfg))
+            if n == 0:
+                raise RetopkError("retopk_workspace_bytes: invalid configuration")
+            self.workspace = torch.empty(int(n) + 256, dtype=torch.uint8, device=device)
+            wp = (self.workspace.data_ptr() + 255) // 256 * 256
+            _check(lib.retopk_create(ctypes.byref(self.cfg), ctypes.c_void_p(wp), int(n), ctypes.byref(h)),
+                   "retopk_create")
+        else:
+            ns = lib.retopk_state_workspace_bytes(ctypes.byref(self.cfg))
+            if ns == 0:
+                raise RetopkError("retopk_state_workspace_bytes: invalid configuration")
+            self.workspace = torch.empty(int(ns) + 256, dtype=torch.uint8, device=device)
+            self.scratch = scratch
+            wp = (self.workspace.data_ptr() + 255) // 256 * 256
+            sp = (scratch.data_ptr() + 255) // 256 * 256
+            avail = scratch.numel() - (sp - scratch.data_ptr())
+            _check(lib.retopk_create_shared(ctypes.byref(self.cfg), ctypes.c_void_p(wp), int(ns), ctypes.c_void_p(sp),
+                                            int(avail), ctypes.byref(h)), "retopk_create_shared")
         self.handle = h
         self.B, self.Hq, self.Hkv, self.max_len = B, Hq, Hkv, max_len
         self.K, self.C, self.W, self.R, self.T_r, self.tau, self.d = K, C, W, R, T_r, tau, d

@@ -22,9 +22,12 @@ def to_dev(a: np.ndarray, device) -> torch.Tensor:
 
 class DecodeRun:
     """`fused` runs each step through retopk_decode_step_kv (append folded into
-    the decision kernel); otherwise retopk_append_kv then retopk_decode_step."""
+    the decision kernel); otherwise retopk_append_kv then retopk_decode_step.
+    `scratch` (a uint8 CUDA tensor) makes the context share its per-step
+    scratch with other contexts (retopk_create_shared)."""
 
-    def __init__(self, w: synth.Workload, arrays=None, device="cuda", max_len=None, fused: bool = True):
+    def __init__(self, w: synth.Workload, arrays=None, device="cuda", max_len=None, fused: bool = True,
+                 scratch=None):
         self.w = w
         self.fused = fused
         self.device = torch.device(device)
@@ -44,7 +47,7 @@ class DecodeRun:
         self.v_new = to_dev(np.ascontiguousarray(v[:, :, L0:].transpose(2, 0, 1, 3)), dev)
         self.out = torch.zeros((B, w.Hq, d), dtype=torch.int16, device=dev)
         self.ctx = ReTopK(B, w.Hq, Hkv, self.max_len, K=w.K, C=w.C, W=w.W, R=w.R, T_r=w.T_r,
-                          tau=w.tau, d=d, device=dev, recent=w.recent)
+                          tau=w.tau, d=d, device=dev, recent=w.recent, scratch=scratch)
         self.ctx.retopk_init_cache(self.q_prompt, self.k_cache, self.seqlens)
         self.t = 0
         self.graph = None
@@ -106,13 +109,13 @@ class DecodeRun:
 class ExactRun:
     """Stateless Exact Top-K steps over the same inputs (the comparison path)."""
 
-    def __init__(self, dr: DecodeRun):
+    def __init__(self, dr: DecodeRun, workspace=None):
         w = dr.w
         self.dr = dr
         self.idx = torch.empty((w.B, w.Hq, w.K), dtype=torch.int32, device=dr.device)
         self.out = torch.empty((w.B, w.Hq, w.d), dtype=torch.int16, device=dr.device)
         nb = exact_topk_workspace_bytes(w.B, w.Hq, w.Hkv, w.d, dr.max_len, w.K)
-        self.ws = torch.empty(nb + 256, dtype=torch.uint8, device=dr.device)
+        self.ws = workspace if workspace is not None else torch.empty(nb + 256, dtype=torch.uint8, device=dr.device)
 
     def step(self, q, stream=None, seqlens=None):
         dr = self.dr

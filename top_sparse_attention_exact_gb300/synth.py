@@ -106,6 +106,13 @@ def batched_sweep(K: int, tau: float, steps: int = 256) -> Workload:
                     tau, 128, 64, 256, 0.80, tuple(range(100, 116)))
 
 
+# the batch-16 64K sweep: K in {256, 1024, 2048} x tau in {0.70, 0.95}
+for _K in (256, 1024, 2048):
+    for _tau in (0.70, 0.95):
+        _w = batched_sweep(_K, _tau)
+        WORKLOADS[_w.name] = _w
+
+
 def scaled(w: Workload, **kw) -> Workload:
     """Same recipe with some fields replaced (smaller parity cases)."""
     d = dict(w.__dict__)
