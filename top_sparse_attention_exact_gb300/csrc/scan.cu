@@ -167,6 +167,7 @@ __device__ __forceinline__ int row_perm(int g) { return (g & 4) | ((g & 1) << 1)
 struct ScanShared {
     uint64_t full[8];
     uint64_t empty[8];
+    int timed_out;                  // a pipeline wait expired (copies may still be in flight)
     int n_groups;
     int total_tiles;
     int grp_first[kMaxGroups + 1];  // prefix of tiles over groups b * Hkv + hk
@@ -194,6 +195,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             mbar_init(&sh.empty[s2], kConsumerWarps);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        sh.timed_out = 0;
     }
     // Without a path decision (the stateless exact step, cache initialisation)
     // nothing the tiles or the tile list read comes from the previous kernel
@@ -270,6 +272,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 mbar_expect_tx(&sh.full[s], kStageBytes);
                 tma_load_2d(dst, &kmap, 0, 2 * row, &sh.full[s], policy);
             }
+            if (!ok)
+                sh.timed_out = 1;
         }
     } else {
         // ================= consumers =================
@@ -382,11 +386,14 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                        tid);
         if (nonfinite)
             atomicOr(a.status, RETOPK_STATUS_NONFINITE);
+        if (!ok)
+            sh.timed_out = 1;
     }
     __syncthreads();
-    // Drain: every issued copy has landed before shared memory is released
-    // (immediate on the normal path, where the consumers waited on each one).
-    if (tid == kConsumerWarps * 32) {
+    // Drain: every issued copy has landed before shared memory is released.
+    // On the normal path the consumers waited on each one; only after an
+    // expired wait can copies still be in flight.
+    if (tid == kConsumerWarps * 32 && sh.timed_out) {
         const int n = t_end - t_begin;
         for (int s = 0; s < S && s < n; ++s) {
             const int last = s + ((n - 1 - s) / S) * S;     // last issue index that used stage s
