@@ -519,14 +519,22 @@ def our_arm(args, w, rank, world, dist):
         kn = torch.from_numpy(np.ascontiguousarray(arrays[0][:, :, wr.L0:].transpose(2, 0, 1, 3)).view(np.int16)).pin_memory()
         vn = torch.from_numpy(np.ascontiguousarray(arrays[1][:, :, wr.L0:].transpose(2, 0, 1, 3)).view(np.int16)).pin_memory()
         out_h = torch.empty((wr.steps, wr.B, wr.Hq, wr.d), dtype=torch.int16).pin_memory()
-        # one host view per step and buffer, made before the timed loop (a caller
-        # holds its own per-token host tensors)
-        views = [(kn[t], vn[t], qh[t], out_h[t]) for t in range(wr.steps)]
+        # the C ABI entry point with host buffers, called as a C caller would:
+        # its per-token host buffers' addresses are known before the loop
+        import ctypes
+        fn = retopk.load().retopk_decode_step_host
+        dev_args = (de.ctx.handle, None, None, None, ctypes.c_void_p(de.k_cache.data_ptr()),
+                    ctypes.c_void_p(de.v_cache.data_ptr()), ctypes.c_void_p(de.seqlens.data_ptr()), None,
+                    ctypes.c_void_p(stream.cuda_stream))
+        ptrs = [(ctypes.c_void_p(kn[t].data_ptr()), ctypes.c_void_p(vn[t].data_ptr()),
+                 ctypes.c_void_p(qh[t].data_ptr()), ctypes.c_void_p(out_h[t].data_ptr())) for t in range(wr.steps)]
 
         def e2e_step(t):
             # host buffers in, host buffer out: the library stages them and replays the step's graph
-            k1, v1, q1, o1 = views[t]
-            de.ctx.retopk_decode_step_host(k1, v1, q1, de.k_cache, de.v_cache, de.seqlens, o1, stream)
+            k1, v1, q1, o1 = ptrs[t]
+            rc = fn(dev_args[0], k1, v1, q1, dev_args[4], dev_args[5], dev_args[6], o1, dev_args[8])
+            if rc:
+                raise RuntimeError(f"retopk_decode_step_host failed ({rc})")
 
         for t in range(Wm):
             e2e_step(t)
@@ -544,8 +552,9 @@ def our_arm(args, w, rank, world, dist):
         e2e = {"value": float(np.mean(e_ms) * 1000.0), "unit": UNIT,
                "h2d_bytes_per_step": int(qh[0].numel() * 2 + kn[0].numel() * 2 + vn[0].numel() * 2),
                "d2h_bytes_per_step": int(out_h[0].numel() * 2),
-               "how": "retopk_decode_step_host per step (C ABI, host buffers): pinned-host inputs copied in, "
-                      "the decode step replayed as the library's graph, the output copied out, synchronised"}
+               "how": "retopk_decode_step_host per step, called through the C ABI (ctypes, host-buffer "
+                      "addresses prepared before the loop): pinned-host inputs copied in, the decode step "
+                      "replayed as the library's graph, the output copied out, synchronised"}
         del de
 
     # ---- CPU oracle baseline on a bounded sample (rank 0 only) --------------------
