@@ -152,6 +152,64 @@ __device__ __forceinline__ void filter_masks(const uint4 *s4, int nblk, int ng, 
     }
 }
 
+// ---- the select's rare paths, kept out of line -----------------------------
+// They run only when many keys tie at the 19-bit prefix, when the histograms
+// disagree with the scores, or for long histories.  Out of line, the common
+// path's code stays short and contiguous: after an L2 flush a lone exact
+// head's cluster fetches it from device memory phase by phase.
+
+// The threshold of the `need` largest staged candidates by the full radix
+// select (no usable second digit).
+static __device__ __noinline__ unsigned long long staged_full_select(int N2, int need, const int32_t *st_idx,
+                                                              const uint32_t *st_key, SelectShared &sel)
+{
+    auto get = [&](int j, int32_t &idx, uint32_t &k) {
+        idx = st_idx[j];
+        k = st_key[j];
+    };
+    return radix_select_threshold<kSelThreads>(N2, need, get, sel);
+}
+
+// The threshold among the staged candidates sharing the 19-bit prefix when
+// more than 32 share it: radix refinement below the prefix.
+static __device__ __noinline__ unsigned long long staged_refine(int N2, int rem, uint32_t p19, const int32_t *st_idx,
+                                                         const uint32_t *st_key, SelectShared &sel)
+{
+    auto get = [&](int j, int32_t &idx, uint32_t &k) {
+        idx = st_idx[j];
+        k = st_key[j];
+    };
+    return radix_refine<kSelThreads>(N2, rem, (unsigned long long)p19 << (32 + kSub), 32 + kSub, get, sel);
+}
+
+// More final candidates than the staging holds: select among all candidates in
+// place, in the global segments (offsets off[] of the unfiltered per-rank
+// lists), compact the support into sup_i / sup_k and leave its maximum key in
+// kmax.  Returns the support's length.
+static __device__ __noinline__ int global_select(int N, int need, int K, int seg, const int *off, const int32_t *gi,
+                                          const uint32_t *gk, int32_t *sup_i, uint32_t *sup_k, SelectShared &sel,
+                                          uint32_t *kmax)
+{
+    auto get = [&](int j, int32_t &idx, uint32_t &k) {
+        int r = 0;
+        while (r + 1 < kExactCluster && off[r + 1] <= j)
+            ++r;
+        const int o = r * seg + (j - off[r]);
+        idx = gi[o];
+        k = gk[o];
+    };
+    const unsigned long long thr = radix_select_threshold<kSelThreads>(N, need, get, sel);
+    const int n = stable_compact<kSelThreads, 4>(N, thr, get, K, sup_i, sup_k, sel.warp_tot);
+    __syncthreads();
+    uint32_t km = 0u;
+    for (int j = threadIdx.x; j < n; j += kSelThreads)
+        km = max(km, sup_k[j]);
+    km = __reduce_max_sync(0xffffffffu, km);
+    if ((threadIdx.x & 31) == 0)
+        atomicMax(kmax, km);
+    return n;
+}
+
 // One exact-path head per cluster of kExactCluster CTAs of kSelThreads
 // threads; `smem` is the CTA's dynamic shared memory (sel_smem_bytes).
 __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned char *smem)
@@ -482,12 +540,6 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
             atomicMax(&sh.kmax, km);
     }
     __syncthreads();
-    auto goff = [&](int j) {
-        int r = 0;
-        while (r + 1 < kExactCluster && sh.off[r + 1] <= j)
-            ++r;
-        return r * seg + (j - sh.off[r]);
-    };
     auto get_staged = [&](int j, int32_t &idx, uint32_t &k) {
         idx = st_idx[j];
         k = st_key[j];
@@ -525,12 +577,10 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
                 __syncthreads();
             }
         }
-        thr =
-            N2 <= need                        ? 0ull
-            : sh.above2 < 0                   ? radix_select_threshold<kSelThreads>(N2, need, get_staged, sh.sel)
-            : sh.ntie <= 32                   ? sh.tie_thr
-                                              : radix_refine<kSelThreads>(N2, rem, (unsigned long long)p19 << (32 + kSub),
-                                                                          32 + kSub, get_staged, sh.sel);
+        thr = N2 <= need         ? 0ull
+              : sh.above2 < 0    ? staged_full_select(N2, need, st_idx, st_key, sh.sel)
+              : sh.ntie <= 32    ? sh.tie_thr
+                                 : staged_refine(N2, rem, p19, st_idx, st_key, sh.sel);
         n = stable_compact<kSelThreads, 4>(N2, thr, get_staged, w.K, sup_i, sup_k, sh.sel.warp_tot);
     } else {
         // more than kSelStageCap final candidates: select among all of them
@@ -544,20 +594,7 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
             sh.off[kExactCluster] = acc;
         }
         __syncthreads();
-        auto get_global = [&](int j, int32_t &idx, uint32_t &k) {
-            const int o = goff(j);
-            idx = gi[o];
-            k = gk[o];
-        };
-        thr = radix_select_threshold<kSelThreads>(N, need, get_global, sh.sel);
-        n = stable_compact<kSelThreads, 4>(N, thr, get_global, w.K, sup_i, sup_k, sh.sel.warp_tot);
-        __syncthreads();
-        uint32_t km = 0u;
-        for (int j = tid; j < n; j += kSelThreads)
-            km = max(km, sup_k[j]);
-        km = __reduce_max_sync(0xffffffffu, km);
-        if (lane == 0)
-            atomicMax(&sh.kmax, km);
+        n = global_select(N, need, w.K, seg, sh.off, gi, gk, sup_i, sup_k, sh.sel, &sh.kmax);
     }
     __syncthreads();
     const float m = key2f(sh.kmax);
