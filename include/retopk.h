@@ -60,6 +60,10 @@ enum {
 #define RETOPK_STATUS_NONFINITE   0x4u  /* a non-finite score was produced          */
 #define RETOPK_STATUS_TIMEOUT     0x8u  /* a bounded pipeline wait expired (the step's
                                            results are not valid)                  */
+#define RETOPK_STATUS_GATHER      0x10u /* a gathered K/V row index outside [0, L) was
+                                          skipped: checked by builds with
+                                          RETOPK_CHECKED defined, and always by
+                                          retopk_fidelity (against max_len)      */
 
 /* Path codes reported per (sequence, query head), Eq. (13). */
 #define RETOPK_PATH_REUSE    0
@@ -226,7 +230,12 @@ int retopk_get_counters(retopk_ctx *ctx, int64_t counts[5], void *stream);
  *   fifo_len [B, Hq, C]     int32
  *   seq      [B, 3]         int32  (next slot, live count, t_dec)
  * Live entry c (0 = oldest) of sequence b sits in slot
- * (seq[b][0] - seq[b][1] + c) mod C.  Both calls synchronise `stream`. */
+ * (seq[b][0] - seq[b][1] + c) mod C.  Both calls synchronise `stream`.
+ * Import refuses (RETOPK_ERR_STATE, device untouched) a slot or count out of
+ * range, a length outside [0, K], and a support whose first `len` entries are
+ * not strictly ascending and nonnegative; a support index at or beyond the
+ * sequence's current length is reported when a step reads it
+ * (RETOPK_STATUS_BAD_INDEX) and left out of the candidates. */
 size_t retopk_state_bytes(const retopk_ctx *ctx);
 int retopk_export_state(retopk_ctx *ctx, void *host_buf, size_t bytes, void *stream);
 int retopk_import_state(retopk_ctx *ctx, const void *host_buf, size_t bytes, void *stream);
@@ -329,7 +338,9 @@ int exact_topk_attention_step_noalloc(const retopk_bf16 *q, const retopk_bf16 *k
  *   [2] cosine of the two head outputs,
  *   [3] cosine of the two attention distributions.
  * exact_idx: [B, Hq, K] int32 ascending, -1 padded; out / out_exact / q:
- * [B, Hq, d] bf16.  A diagnostic beside the decode loop, not part of it. */
+ * [B, Hq, d] bf16.  An exact_idx entry outside [0, max_len) is not read (it
+ * scores 0) and sets RETOPK_STATUS_GATHER in the context's status word.
+ * A diagnostic beside the decode loop, not part of it. */
 int retopk_fidelity(retopk_ctx *ctx, const retopk_bf16 *q, const retopk_bf16 *k_cache, const int32_t *exact_idx,
                     const retopk_bf16 *out_exact, const retopk_bf16 *out, float *metrics, void *stream);
 

@@ -30,6 +30,15 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) == set(retopk.EXPORTED)
 
 
+def test_checked_build_exports_every_entry_point():
+    # the RETOPK_CHECKED variant (gathered row indices range-checked) builds
+    # and carries the same ABI
+    from top_sparse_attention_exact_gb300 import _build
+    chk = ctypes.CDLL(_build.build(checked=True))
+    for n in declared_functions():
+        assert hasattr(chk, n), n
+
+
 def test_config_validation_without_gpu(lib):
     ok = retopk.retopk_config(1, 28, 4, 128, 131584, 512, 32, 32, 4, 128, 0.85)
     assert lib.retopk_workspace_bytes(ctypes.byref(ok)) > 0

@@ -505,9 +505,14 @@ def test_state_round_trip_and_status_bits():
     st2 = dr.ctx.retopk_export_state()
     for key in st:
         assert np.array_equal(st[key], st2[key])
-    # a support index beyond the history is reported, not followed
+    # a support index beyond the history is reported, not followed (the last
+    # live entry of every cached support: the lists stay ascending)
     bad = {k: v.copy() for k, v in st.items()}
-    bad["fifo_sup"][0, :, :, 0] = 10 ** 6
+    lens = bad["fifo_len"][0]
+    assert (lens > 0).all()
+    for h in range(lens.shape[0]):
+        for c in range(lens.shape[1]):
+            bad["fifo_sup"][0, h, c, lens[h, c] - 1] = 10 ** 6
     dr.ctx.retopk_import_state(bad)
     dr.ctx.retopk_decode_step(dr.q_dec[1], dr.k_cache, dr.v_cache, dr.seqlens, dr.out)
     s = dr.ctx.retopk_get_status(clear=True)
@@ -524,12 +529,20 @@ def test_state_round_trip_and_status_bits():
     dr.ctx.retopk_decode_step_kv(dr.k_new[0], dr.v_new[0], dr.q_dec[2], dr.k_cache, dr.v_cache, dr.seqlens, dr.out)
     assert dr.ctx.retopk_get_status() & 0x2
     assert (dr.seqlens.cpu() == dr.max_len).all()
-    # malformed state buffers are refused on the host
-    bad = {k: v.copy() for k, v in st.items()}
-    bad["seq"][0, 0] = w.C
+    # malformed state buffers are refused on the host: a slot out of range, a
+    # support out of order, a negative support index
     from top_sparse_attention_exact_gb300.retopk import RetopkError
-    with pytest.raises(RetopkError):
-        dr.ctx.retopk_import_state(bad)
+    for what in ("slot", "order", "negative"):
+        bad = {k: v.copy() for k, v in st.items()}
+        if what == "slot":
+            bad["seq"][0, 0] = w.C
+        elif what == "order":
+            s0 = bad["fifo_sup"][0, 3, 1]
+            s0[0], s0[1] = s0[1], s0[0]
+        else:
+            bad["fifo_sup"][0, 3, 1, 0] = -5
+        with pytest.raises(RetopkError):
+            dr.ctx.retopk_import_state(bad)
 
 
 def test_nonfinite_scores_are_reported():

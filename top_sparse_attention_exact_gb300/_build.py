@@ -3,6 +3,11 @@
 Compiles every ``csrc/*.cu`` file in parallel with nvcc and links them into
 ``_build/libretopk.so``.  No cmake, no torch extension machinery: the library
 exposes a plain C ABI (include/retopk.h) that the ctypes binding loads.
+
+``build(checked=True)`` makes ``_build/checked/libretopk_checked.so``, the same
+library compiled with ``RETOPK_CHECKED`` defined: every K / V row a kernel
+gathers is range-checked against the sequence length first (a violation sets
+RETOPK_STATUS_GATHER and the row is skipped).
 """
 from __future__ import annotations
 
@@ -17,6 +22,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libretopk.so")
+CHECKED_DIR = os.path.join(OUT_DIR, "checked")
+LIB_CHECKED = os.path.join(CHECKED_DIR, "libretopk_checked.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -36,24 +43,28 @@ def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + [os.path.join(ROOT, "include", "retopk.h")]
     return any(os.path.getmtime(p) > t for p in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    """Compile (if stale) and return the path of libretopk.so."""
-    if not force and not _stale():
-        return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra=(), checked: bool = False) -> str:
+    """Compile (if stale) and return the path of libretopk.so (of
+    libretopk_checked.so with checked=True)."""
+    lib, out_dir = (LIB_CHECKED, CHECKED_DIR) if checked else (LIB, OUT_DIR)
+    if checked:
+        extra = (*extra, "-DRETOPK_CHECKED")
+    if not force and not _stale(lib):
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
     objs = []
 
     def one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *_flags(extra), "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -64,12 +75,12 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(one, sources()))
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = lib + f".{os.getpid()}.tmp"
     r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -681,8 +681,8 @@ int retopk_fidelity(retopk_ctx *ctx, const retopk_bf16 *q, const retopk_bf16 *k_
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(out_exact) || !aligned16(out))
         return RETOPK_ERR_ALIGN;
     const Work &w = ctx->w;
-    return cuda_rc(launch_fidelity(q, k_cache, exact_idx, w.support, out_exact, out, metrics, w.B, w.Hq, w.Hkv,
-                                   w.max_len, w.K, (cudaStream_t)stream));
+    return cuda_rc(launch_fidelity(q, k_cache, exact_idx, w.support, out_exact, out, metrics, w.status, w.B, w.Hq,
+                                   w.Hkv, w.max_len, w.K, (cudaStream_t)stream));
 }
 
 int retopk_support_overlap(const int32_t *S, const int32_t *others, int rows, int R, int K, float *out,
@@ -826,9 +826,18 @@ int retopk_import_state(retopk_ctx *ctx, const void *host_buf, size_t bytes, voi
     const char *p = (const char *)host_buf;
     const int32_t *len = (const int32_t *)(p + BHC * kD * 2 + BHC * w.K * 4);
     const int32_t *seq = len + BHC;
-    for (size_t i = 0; i < BHC; ++i)
+    const int32_t *sup = (const int32_t *)(p + BHC * kD * 2);
+    for (size_t i = 0; i < BHC; ++i) {
         if (len[i] < 0 || len[i] > w.K)
             return RETOPK_ERR_STATE;
+        // a support is a set of key positions, stored ascending
+        const int32_t *si = sup + i * w.K;
+        if (len[i] > 0 && si[0] < 0)
+            return RETOPK_ERR_STATE;
+        for (int j = 1; j < len[i]; ++j)
+            if (si[j] <= si[j - 1])
+                return RETOPK_ERR_STATE;
+    }
     for (int b = 0; b < w.B; ++b)
         if (seq[b * 3] < 0 || seq[b * 3] >= w.C || seq[b * 3 + 1] < 0 || seq[b * 3 + 1] > w.C ||
             seq[b * 3 + 2] < 0)

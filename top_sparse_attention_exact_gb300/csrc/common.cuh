@@ -198,6 +198,24 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
                  : "memory");
 }
 
+// Range check of a gathered K / V row.  A build with RETOPK_CHECKED defined
+// checks every row index a kernel gathers against the sequence's length
+// before the load; a violation sets RETOPK_STATUS_GATHER and the row is
+// skipped (read as zeros), never a trap.  Other builds compile the check away:
+// every gathered index comes from a scan or a candidate list over [0, L).
+#ifdef RETOPK_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+__device__ __forceinline__ bool row_ok(int32_t idx, int L, uint32_t *status)
+{
+    if (!kChecked || (uint32_t)idx < (uint32_t)L)
+        return true;
+    atomicOr(status, RETOPK_STATUS_GATHER);
+    return false;
+}
+
 // Effective length of sequence b for a launch (len_off < 0 during cache
 // initialisation, where the causal prefix of a prompt position is scored).
 // Clamped to the cache capacity so that a bad length can never index past it.
@@ -221,8 +239,8 @@ cudaError_t launch_exact_select(const Work &w, QSrc q, const uint16_t *v_cache, 
                                 int len_off, int mode, int init_slot, uint16_t *out, int32_t *idx_out,
                                 cudaStream_t st);
 cudaError_t launch_fidelity(const uint16_t *q, const uint16_t *k, const int32_t *S, const int32_t *Sh,
-                            const uint16_t *o, const uint16_t *oh, float *out, int B, int Hq, int Hkv,
-                            int max_len, int K, cudaStream_t st);
+                            const uint16_t *o, const uint16_t *oh, float *out, uint32_t *status, int B, int Hq,
+                            int Hkv, int max_len, int K, cudaStream_t st);
 cudaError_t launch_overlap(const int32_t *S, const int32_t *others, int rows, int R, int K, float *out,
                            cudaStream_t st);
 cudaError_t launch_decide(const Work &w, const uint16_t *q, uint16_t *q_copy, const uint16_t *k_new,

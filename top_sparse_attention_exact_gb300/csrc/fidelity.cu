@@ -10,7 +10,10 @@
 //   m[1] retained mass       sum over Sh n S of p, p = softmax over S
 //   m[2] output cosine       cos(oh, o) of the two bf16 head outputs
 //   m[3] distribution cosine sum over Sh n S of p ph / (|p| |ph|)
-// are written in fp32.
+// are written in fp32.  The supports come from the caller: an entry outside
+// [0, max_len) (other than the -1 padding after the valid ones) would address
+// past the cache, so its row is not read; it scores 0 and sets
+// RETOPK_STATUS_GATHER.
 #include "common.cuh"
 
 namespace retopk {
@@ -26,6 +29,7 @@ struct FidArgs {
     const uint16_t *o;       // [B, Hq, d] exact output
     const uint16_t *oh;      // [B, Hq, d] judged output
     float *out;              // [B, Hq, 4]
+    uint32_t *status;
     int Hq, Hkv, max_len, K;
     float scale;
 };
@@ -83,7 +87,10 @@ __global__ void __launch_bounds__(kFidThreads) fidelity_kernel(FidArgs a)
     const uint2 qr = *reinterpret_cast<const uint2 *>(a.q + (size_t)bh * kD + lane * 4);
     for (int j = warp; j < nS + nh; j += kFidWarps) {
         const int row = j < nS ? S[j] : Sh[j - nS];
-        const uint2 kr = *reinterpret_cast<const uint2 *>(kb + (size_t)row * kD + lane * 4);
+        const bool in = (uint32_t)row < (uint32_t)a.max_len;
+        if (!in && lane == 0)
+            atomicOr(a.status, RETOPK_STATUS_GATHER);
+        const uint2 kr = in ? *reinterpret_cast<const uint2 *>(kb + (size_t)row * kD + lane * 4) : make_uint2(0u, 0u);
         float e = bf16lo(qr.x) * bf16lo(kr.x) + bf16hi(qr.x) * bf16hi(kr.x) + bf16lo(qr.y) * bf16lo(kr.y) +
                   bf16hi(qr.y) * bf16hi(kr.y);
         e = warp_sum(e) * a.scale;
@@ -173,10 +180,10 @@ __global__ void __launch_bounds__(kFidThreads) fidelity_kernel(FidArgs a)
 }
 
 cudaError_t launch_fidelity(const uint16_t *q, const uint16_t *k, const int32_t *S, const int32_t *Sh,
-                            const uint16_t *o, const uint16_t *oh, float *out, int B, int Hq, int Hkv,
-                            int max_len, int K, cudaStream_t st)
+                            const uint16_t *o, const uint16_t *oh, float *out, uint32_t *status, int B, int Hq,
+                            int Hkv, int max_len, int K, cudaStream_t st)
 {
-    FidArgs a{q, k, S, Sh, o, oh, out, Hq, Hkv, max_len, K, 1.0f / sqrtf((float)kD)};
+    FidArgs a{q, k, S, Sh, o, oh, out, status, Hq, Hkv, max_len, K, 1.0f / sqrtf((float)kD)};
     fidelity_kernel<<<B * Hq, kFidThreads, (size_t)K * 16, st>>>(a);
     return cudaGetLastError();
 }

@@ -52,6 +52,7 @@ struct ReuseArgs {
 
 struct ReuseShared {
     float qf[kD];
+    int len_c[kMaxC];      // support length of every cache slot
     int pre[kMaxC + 1];    // prefix of the retrieved supports' lengths
     int sup_off[kMaxC];    // cache offset of each retrieved support
     int wcount[kReuseWarps];
@@ -129,12 +130,17 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
         sh.qf[tid] = __uint_as_float(((uint32_t)a.q[(size_t)bh * kD + tid]) << 16);
     if (rank == 0 && tid < kD / 8)   // q_t into its slot, off the critical path (only the decision reads fifo_q)
         reinterpret_cast<uint4 *>(w.fifo_q + e_slot * kD)[tid] = reinterpret_cast<const uint4 *>(a.q + (size_t)bh * kD)[tid];
+    // the retrieved positions and every slot's support length, loaded side by
+    // side (not the lengths after the positions: one round trip, not two)
+    const int pos_r = tid < w.R ? w.topR[(size_t)bh * w.R + tid] : 0;
+    if (tid < w.C)
+        sh.len_c[tid] = w.fifo_len[(size_t)bh * w.C + tid];
+    __syncthreads();
     {   // slots, lengths and prefix of the nr (<= C <= kReuseThreads) retrieved supports
         int len = 0, off = 0;
         if (tid < nr) {
-            const int pos = w.topR[(size_t)bh * w.R + tid];
-            const int slot = ((head - count + pos) % w.C + w.C) % w.C;
-            len = w.fifo_len[(size_t)bh * w.C + slot];
+            const int slot = ((head - count + pos_r) % w.C + w.C) % w.C;
+            len = sh.len_c[slot];
             off = (int)(((size_t)bh * w.C + slot) * w.K);
         }
         int tot;
@@ -322,8 +328,9 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
 #pragma unroll
             for (int u = 0; u < kRerankRows; ++u) {
                 const int j = jb + hw + u * kHalfWarps;
-                kv[u] = (j < ce) ? reinterpret_cast<const uint4 *>(kb + (size_t)cand[j] * kD)[hl]
-                                 : make_uint4(0u, 0u, 0u, 0u);
+                kv[u] = (j < ce && row_ok(cand[j], L, w.status))
+                            ? reinterpret_cast<const uint4 *>(kb + (size_t)cand[j] * kD)[hl]
+                            : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
             for (int u = 0; u < kRerankRows; ++u) {
@@ -398,7 +405,7 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float zsum = 0.f;
     const uint16_t *vb = a.v + ((size_t)(b * w.Hkv + hk) * w.max_len) * kD;
-    value_partial<8>(vb, sup_i, sup_k, vs + warp, ve, kReuseWarps, m, acc, zsum);
+    value_partial<8>(vb, sup_i, sup_k, vs + warp, ve, kReuseWarps, m, acc, zsum, L, w.status);
     *reinterpret_cast<float4 *>(&tl.red[warp][lane * 4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     if (lane == 0)
         tl.zw[warp] = zsum;

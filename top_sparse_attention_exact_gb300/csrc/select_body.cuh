@@ -628,7 +628,7 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     if (a.mode != FIN_INIT) {   // cache initialisation needs the support only
         const int vper = (n + kExactCluster - 1) / kExactCluster;
         const int vs = min(n, rank * vper), ve = min(n, vs + vper);
-        value_partial<8>(vb, sup_i, sup_k, vs + warp, ve, kSelWarps, m, acc, zsum);
+        value_partial<8>(vb, sup_i, sup_k, vs + warp, ve, kSelWarps, m, acc, zsum, L, w.status);
     }
     *reinterpret_cast<float4 *>(&red[warp][lane * 4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     if (lane == 0)

@@ -212,10 +212,12 @@ __device__ int stable_compact(int N, unsigned long long thr, Get get, int cap, i
 
 // Softmax-weighted partial sum over support rows [j0, j1) (stride `step` per
 // warp): lane l accumulates dims 4l..4l+3 with weights exp(score - m).
-// U rows in flight per lane.
+// U rows in flight per lane.  L and status serve the checked build's range
+// check of the row indices (row_ok).
 template <int U = 16>
 __device__ __forceinline__ void value_partial(const uint16_t *vb, const int32_t *sup_i, const uint32_t *sup_k,
-                                              int j0, int j1, int step, float m, float (&acc)[4], float &zsum)
+                                              int j0, int j1, int step, float m, float (&acc)[4], float &zsum,
+                                              int L, uint32_t *status)
 {
     const int lane = threadIdx.x & 31;
     for (int jb = j0; jb < j1; jb += step * U) {
@@ -224,7 +226,7 @@ __device__ __forceinline__ void value_partial(const uint16_t *vb, const int32_t 
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int j = jb + u * step;
-            if (j < j1) {
+            if (j < j1 && row_ok(sup_i[j], L, status)) {
                 vv[u] = *reinterpret_cast<const uint2 *>(vb + (size_t)sup_i[j] * kD + lane * 4);
                 p[u] = expf(key2f(sup_k[j]) - m);
             } else {

@@ -19,7 +19,7 @@ from . import _build
 _lib = None
 
 RETOPK_PATH_REUSE, RETOPK_PATH_FALLBACK, RETOPK_PATH_REFRESH = 0, 1, 2
-STATUS_BAD_INDEX, STATUS_KV_FULL, STATUS_NONFINITE = 0x1, 0x2, 0x4
+STATUS_BAD_INDEX, STATUS_KV_FULL, STATUS_NONFINITE, STATUS_TIMEOUT, STATUS_GATHER = 0x1, 0x2, 0x4, 0x8, 0x10
 
 EXPORTED = ("retopk_workspace_bytes", "retopk_create", "retopk_destroy", "retopk_init_cache",
             "retopk_append_kv", "retopk_decode_step", "retopk_decode_step_kv", "retopk_get_diagnostics",
