@@ -52,7 +52,6 @@ struct ReuseArgs {
 
 struct ReuseShared {
     float qf[kD];
-    int len_c[kMaxC];      // support length of every cache slot
     int pre[kMaxC + 1];    // prefix of the retrieved supports' lengths
     int sup_off[kMaxC];    // cache offset of each retrieved support
     int wcount[kReuseWarps];
@@ -130,17 +129,12 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
         sh.qf[tid] = __uint_as_float(((uint32_t)a.q[(size_t)bh * kD + tid]) << 16);
     if (rank == 0 && tid < kD / 8)   // q_t into its slot, off the critical path (only the decision reads fifo_q)
         reinterpret_cast<uint4 *>(w.fifo_q + e_slot * kD)[tid] = reinterpret_cast<const uint4 *>(a.q + (size_t)bh * kD)[tid];
-    // the retrieved positions and every slot's support length, loaded side by
-    // side (not the lengths after the positions: one round trip, not two)
-    const int pos_r = tid < w.R ? w.topR[(size_t)bh * w.R + tid] : 0;
-    if (tid < w.C)
-        sh.len_c[tid] = w.fifo_len[(size_t)bh * w.C + tid];
-    __syncthreads();
     {   // slots, lengths and prefix of the nr (<= C <= kReuseThreads) retrieved supports
         int len = 0, off = 0;
         if (tid < nr) {
-            const int slot = ((head - count + pos_r) % w.C + w.C) % w.C;
-            len = sh.len_c[slot];
+            const int pos = w.topR[(size_t)bh * w.R + tid];
+            const int slot = ((head - count + pos) % w.C + w.C) % w.C;
+            len = w.fifo_len[(size_t)bh * w.C + slot];
             off = (int)(((size_t)bh * w.C + slot) * w.K);
         }
         int tot;
