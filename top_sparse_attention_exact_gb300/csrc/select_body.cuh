@@ -224,7 +224,9 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     const int path = (a.mode == FIN_DECODE) ? w.path[bh] : RETOPK_PATH_FALLBACK;
     if (path == RETOPK_PATH_REUSE)
         return;                                    // a reuse head (uniform over the cluster)
-    pdl_wait();                                    // the scan's scores and histogram
+    // Until the wait for the scan below, only what the scan does not write:
+    // the lengths, the ring snapshot and q (written before the scan passed its
+    // own wait, or by the caller before the step), and shared-memory set-up.
     const bool insert = a.mode == FIN_DECODE || a.mode == FIN_INIT;   // into the query-support cache
     const size_t e_slot = insert ? (size_t)bh * w.C + (a.mode == FIN_INIT ? a.init_slot : w.snap[b * SEQ_WORDS + SEQ_HEAD])
                                  : 0;
@@ -264,6 +266,7 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     if (tid < kSubBins)
         sh.h2[tid] = 0u;
     __syncthreads();
+    pdl_wait();                                    // the scan's scores and histogram
     // copies [c0, c0 + n & ~3) by TMA; the <= 3 trailing scores by plain loads
     auto issue = [&](int c0, int n) {
         const int nb = n & ~3;
