@@ -95,6 +95,15 @@ typedef struct retopk_config {
                              RETOPK_RETRIEVE_RECENT (1): the R most recent
                              entries, rho_max over them (the paper's Table 3
                              "recent-R retrieval" ablation)                  */
+    int32_t cluster;      /* CTAs per head in the step's back end (reuse body
+                             and exact select): 0 chooses -- the largest of
+                             8, 4, 2, 1 for which one wave of B*Hq clusters
+                             fits the GPU at two CTAs per SM, raised while
+                             the reuse path's candidate bitmap (L / cluster
+                             positions per CTA) would not fit its shared
+                             memory; or 1, 2, 4, 8 to fix it.  Results do not
+                             depend on it.  The stateless exact step chooses
+                             the same way for its B*Hq heads.            */
 } retopk_config;
 #define RETOPK_RETRIEVE_SIMILAR 0
 #define RETOPK_RETRIEVE_RECENT  1

@@ -21,8 +21,8 @@ from top_sparse_attention_exact_gb300.runner import DecodeRun, ExactRun
 pytestmark = pytest.mark.gpu
 
 
-def run_checked(w, check_steps=None, arrays=None, max_len=None):
-    dr = DecodeRun(w, arrays=arrays, max_len=max_len)
+def run_checked(w, check_steps=None, arrays=None, max_len=None, cluster=0):
+    dr = DecodeRun(w, arrays=arrays, max_len=max_len, cluster=cluster)
     k, v, qd = dr.k_host, dr.v_host, dr.qd_host
     errs, agg = [], dict(path_band=0, topR_band=0, swaps=0, heads=0)
     paths = []
@@ -151,6 +151,31 @@ def test_batched_sweep_sampled(sweep_arrays, K, tau):
     assert not errs, "\n".join(errs[:20])
     p = np.concatenate(paths)
     assert (p[-2 * w.B * w.Hq:-w.B * w.Hq] == 2).all()   # step 128 refreshes every head
+
+
+@pytest.mark.parametrize("cluster", [1, 2, 4])
+def test_back_end_cluster_sizes(cluster):
+    # the decode step's back end with 1, 2 or 4 CTAs per head (a sequence of
+    # 28 heads gets 8): every checked step against the oracle, and the same
+    # paths and supports as the 8-CTA context on the same inputs
+    w = synth.scaled(synth.WORKLOADS["qwen7b_16k"], L0=4096, steps=12, T_r=5, name=f"cluster{cluster}")
+    arrays = synth.generate(w)
+    steps = {1, 2, 5, 6, 9, 10, 12}
+    dr, errs, agg, paths = run_checked(w, check_steps=steps, arrays=arrays, cluster=cluster)
+    assert not errs, "\n".join(errs[:20])
+    ref, errs8, _, paths8 = run_checked(w, check_steps=steps, arrays=arrays, cluster=8)
+    assert not errs8
+    p = np.concatenate(paths)
+    assert (p == 0).any() and (p != 0).any()
+    assert np.array_equal(p, np.concatenate(paths8))
+    d, d8 = dr.ctx.retopk_get_diagnostics(), ref.ctx.retopk_get_diagnostics()
+    assert np.array_equal(d["support"], d8["support"]) and np.array_equal(d["M"], d8["M"])
+    for h in np.nonzero(d["path"] == 0)[0]:   # A_t of the reuse heads (exact heads list per CTA)
+        assert np.array_equal(d["cand"][h, :d["M"][h]], d8["cand"][h, :d["M"][h]]), h
+    o = synth.bf16_bits_to_f32(dr.out.cpu().numpy().view(np.uint16))
+    o8 = synth.bf16_bits_to_f32(ref.out.cpu().numpy().view(np.uint16)).astype(np.float64)
+    for h in range(w.Hq):   # the same support, partial sums grouped differently
+        assert out_close(o[0, h], o8[0, h])[0], h
 
 
 @pytest.mark.parametrize("variant", ["W0", "no_fallback"])

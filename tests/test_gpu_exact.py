@@ -170,3 +170,15 @@ def test_exact_headline_128k_sampled_heads():
         assert ok, msg
         ok, mx, rel = out_close(out[0, h], ref)
         assert ok, (h, mx, rel)
+
+
+@pytest.mark.parametrize("B", [2, 5, 16])
+def test_exact_batched_cluster_sizes(B):
+    # 28 query heads per sequence over 4 KV heads: B = 2, 5 and 16 give the
+    # select 4, 2 and 1 CTAs per head (the clusters of one wave), ragged lengths
+    rng = np.random.default_rng(100 + B)
+    L = [int(x) for x in rng.integers(900, 3100, size=B)]
+    q, k, v = gauss(200 + B, B, 28, 4, max(L) + 3)
+    idx, out = run_exact(q, k, v, L, 64, max_len=max(L) + 19)
+    errs = compare_exact(q, k, v, L, 64, idx, out, f"B{B}")
+    assert not errs, "\n".join(errs[:20])

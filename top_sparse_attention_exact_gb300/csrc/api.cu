@@ -15,7 +15,7 @@ namespace retopk {
 cudaError_t configure_scan();
 cudaError_t configure_select();
 cudaError_t configure_finish();
-size_t finish_smem_bytes_for(int max_len, int K, int RKW);
+size_t finish_smem_bytes_for(int max_len, int K, int RKW, int CL);
 cudaError_t configure_fidelity();
 }  // namespace retopk
 
@@ -120,13 +120,34 @@ int ensure_configured()
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
-// Per-head capacity of the candidate arrays: the kExactCluster segments of an
-// exact head (each a multiple of 16 entries) or a reuse head's A_t.
+// Per-head capacity of the candidate arrays: the segments of an exact head
+// (one per CTA of its cluster, each a multiple of 16 entries; the largest over
+// every cluster size, so the workspace does not depend on it) or a reuse
+// head's A_t.
 int cand_stride_for(int max_len, int RKW)
 {
-    const int seg = (((max_len + kExactCluster - 1) / kExactCluster) + 15) & ~15;
-    const int s = std::max(seg * kExactCluster, RKW);
+    int s = RKW;
+    for (int cl = 1; cl <= kExactCluster; cl <<= 1)
+        s = std::max(s, ((((max_len + cl - 1) / cl) + 15) & ~15) * cl);
     return (s + 63) & ~63;
+}
+
+// CTAs per head in the back end (see retopk_config.cluster): the largest of 8,
+// 4, 2, 1 whose B*Hq clusters fit one wave at two CTAs per SM (fewer CTAs per
+// head cost latency per head but save whole waves of clusters once the batch
+// has many heads), raised while the reuse path's shared memory would not fit.
+int cluster_for(const retopk_config &c, bool stateful)
+{
+    if (c.cluster)
+        return c.cluster;
+    const long long heads = (long long)c.batch * c.n_q_heads, slots = 2LL * sm_count();
+    int cl = kExactCluster;
+    while (cl > 1 && heads * cl > slots)
+        cl >>= 1;
+    while (stateful && cl < kExactCluster &&
+           finish_smem_bytes_for(c.max_len, c.K, c.R * c.K + c.W, cl) > kMaxDynSmem)
+        cl <<= 1;
+    return cl;
 }
 
 // The per-context state of a decode context: the query-support cache of
@@ -263,11 +284,16 @@ int check_cfg(const retopk_config *c)
         return e;
     if (c->C < 1 || c->C > kMaxC || c->R < 1 || c->R > c->C || c->W < 0 || c->T_r < 0)
         return RETOPK_ERR_INVALID;
+    if (c->cluster != 0 && c->cluster != 1 && c->cluster != 2 && c->cluster != 4 && c->cluster != 8)
+        return RETOPK_ERR_INVALID;
     if ((long long)c->R * c->K + c->W > kMaxCand)
         return RETOPK_ERR_UNSUPPORTED;
     // the reuse path's bitmap slice and candidate lists share one CTA's shared
-    // memory; the query-support cache is addressed with 32-bit offsets
-    if (finish_smem_bytes_for(c->max_len, c->K, c->R * c->K + c->W) > kMaxDynSmem ||
+    // memory (the slice is smallest with 8 CTAs per head, which the automatic
+    // choice falls back to); the query-support cache is addressed with 32-bit
+    // offsets
+    if (finish_smem_bytes_for(c->max_len, c->K, c->R * c->K + c->W, c->cluster ? c->cluster : kExactCluster) >
+            kMaxDynSmem ||
         (long long)c->batch * c->n_q_heads * c->C * c->K > INT32_MAX)
         return RETOPK_ERR_UNSUPPORTED;
     if (isnan(c->tau))
@@ -422,6 +448,7 @@ int retopk_create_shared(const retopk_config *cfg, void *d_state, size_t state_b
     plan_state(*cfg, &c->w, (char *)d_state);
     plan_scratch(*cfg, true, &c->w, (char *)d_scratch);
     c->w.n_scan = n_scan_for(cfg->batch, cfg->n_kv_heads, cfg->max_len);
+    c->w.cluster = cluster_for(*cfg, true);
     // the state starts at zero; the scratch holds nothing a step reads before writing it
     cudaError_t ce = cudaMemset(d_state, 0, ns);
     if (ce == cudaSuccess)
@@ -454,6 +481,7 @@ int retopk_create(const retopk_config *cfg, void *d_workspace, size_t bytes, ret
     cudaGetDevice(&c->device);
     plan(*cfg, true, &c->w, (char *)d_workspace);
     c->w.n_scan = n_scan_for(cfg->batch, cfg->n_kv_heads, cfg->max_len);
+    c->w.cluster = cluster_for(*cfg, true);
     cudaError_t ce = cudaMemset(d_workspace, 0, plan(*cfg, true, nullptr, nullptr));
     if (ce == cudaSuccess)
         ce = cudaDeviceSynchronize();
@@ -913,6 +941,7 @@ int exact_work(int B, int Hq, int Hkv, int d, int max_len, int K, void *d_worksp
         return e;
     plan(c, false, w, (char *)d_workspace);
     w->n_scan = n_scan_for(B, Hkv, max_len);
+    w->cluster = cluster_for(c, false);
     w->out_f32 = nullptr;
     w->support = nullptr;
     return RETOPK_OK;

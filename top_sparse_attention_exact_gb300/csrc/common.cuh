@@ -37,6 +37,7 @@ struct Work {
     int retrieval;     // RETOPK_RETRIEVE_*
     int cand_stride;   // per-head capacity of cand_idx / cand_key
     int n_scan;        // scan CTAs per (b, h_kv)
+    int cluster;       // CTAs per head in the back end (finish / select kernels): 1, 2, 4 or 8
     int sc_stride;     // row stride of `scores` (max_len rounded up to 16)
     // query-support cache (decode contexts only)
     uint16_t *fifo_q;

@@ -1,23 +1,24 @@
 // reuse_body.cuh -- the reuse path of one decode step for one (sequence,
-// query head) per cluster of kReuseCluster CTAs (ReTopK paper,
+// query head) per cluster of CL CTAs (CL = 1, 2, 4 or 8, at most
+// kReuseCluster; chosen per configuration) (ReTopK paper,
 // §Recall-Before-Rerank Selection, §Reliable Reuse and §Complexity and GPU
 // Implementation: candidate union and dedup, indexed rerank, Top-K, indexed
 // softmax-value aggregation and cache update), after the path decision.
 //
 // The candidate set A_t (Eqs. (8)-(9): window U the retrieved supports) is
 // built through a bitmap over the key positions split across the cluster:
-// rank r owns the positions [r*S, (r+1)*S) (S = L/kReuseCluster rounded up to
+// rank r owns the positions [r*S, (r+1)*S) (S = L/CL rounded up to
 // 32), sets the bits of the window and support entries in that range in its
 // own shared memory, and lists its candidates in ascending order.  After one
 // cluster barrier every rank concatenates the eight lists in rank order
 // (distributed shared memory reads), so the cluster agrees on A_t, ascending.
 // The work that touches HBM is split across the cluster:
-//   Eq. (10) each CTA scores 1/kReuseCluster of the candidate keys (K rows
+//   Eq. (10) each CTA scores 1/CL of the candidate keys (K rows
 //            gathered straight from the cache) and pushes the scores into
 //            every peer's shared memory (distributed shared memory);
 //   Eq. (11) after a cluster barrier each CTA holds all M_t scores and runs
 //            the same radix select -> identical support S_t;
-//   Eq. (12) each CTA aggregates 1/kReuseCluster of the support's V rows with
+//   Eq. (12) each CTA aggregates 1/CL of the support's V rows with
 //            the common max, pushes (sum of weights, weighted sum) to rank 0;
 // after a second barrier rank 0 normalises, writes the output and inserts
 // (q_t, S_t) into the query-support cache (Eq. (5)).
@@ -77,14 +78,14 @@ constexpr int kReuseTailWords = (int)((sizeof(ReuseTail) + 15) / 16 * 4);
 // with A = max(S/32, RKW) rounded up to 4 and Bw = max(RKW, kReuseTailWords).
 constexpr size_t kReuseSharedBytes = (sizeof(ReuseShared) + 127) & ~size_t(127);
 
-// positions per rank of the split bitmap: L / kReuseCluster rounded up to 32
-__host__ __device__ __forceinline__ int reuse_span(int L)
+// positions per rank of the split bitmap: L / CL rounded up to 32
+__host__ __device__ __forceinline__ int reuse_span(int L, int CL)
 {
-    return (((L + kReuseCluster - 1) / kReuseCluster) + 31) & ~31;
+    return (((L + CL - 1) / CL) + 31) & ~31;
 }
-__host__ __device__ __forceinline__ int reuse_words_a(int max_len, int RKW)
+__host__ __device__ __forceinline__ int reuse_words_a(int max_len, int RKW, int CL)
 {
-    const int s = reuse_span(max_len) >> 5;
+    const int s = reuse_span(max_len, CL) >> 5;
     return ((s > RKW ? s : RKW) + 3) & ~3;
 }
 __host__ __device__ __forceinline__ int reuse_words_b(int RKW)
@@ -92,16 +93,18 @@ __host__ __device__ __forceinline__ int reuse_words_b(int RKW)
     return RKW > kReuseTailWords ? RKW : kReuseTailWords;
 }
 
-inline size_t reuse_smem_bytes(int max_len, int RKW)
+inline size_t reuse_smem_bytes(int max_len, int RKW, int CL)
 {
-    return kReuseSharedBytes + ((size_t)reuse_words_a(max_len, RKW) + reuse_words_b(RKW) + (size_t)RKW) * 4;
+    return kReuseSharedBytes + ((size_t)reuse_words_a(max_len, RKW, CL) + reuse_words_b(RKW) + (size_t)RKW) * 4;
 }
 
 // Eqs. (8)-(12) and the cache insertion for one reuse head per cluster of
-// kReuseCluster CTAs of kReuseThreads threads; `smem` is the CTA's dynamic
-// shared memory (reuse_smem_bytes).
+// CL CTAs of kReuseThreads threads; `smem` is the CTA's dynamic shared memory
+// (reuse_smem_bytes).
+template <int CL>
 __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *smem)
 {
+    static_assert(CL == 1 || CL == 2 || CL == 4 || CL == 8, "cluster of 1, 2, 4 or 8 CTAs");
     ReuseShared &sh = *reinterpret_cast<ReuseShared *>(smem);
     uint32_t *rsm = reinterpret_cast<uint32_t *>(smem + kReuseSharedBytes);
     cg::cluster_group cluster = cg::this_cluster();
@@ -112,7 +115,7 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
     if (w.path[bh] != RETOPK_PATH_REUSE)
         return;                                   // uniform over the cluster
     const int RKW = w.R * w.K + w.W;
-    const int wa = reuse_words_a(w.max_len, RKW), wb = reuse_words_b(RKW);
+    const int wa = reuse_words_a(w.max_len, RKW, CL), wb = reuse_words_b(RKW);
     uint32_t *region = rsm;                                           // bitmap slice, then the scores
     uint32_t *keys = region;
     int32_t *loc = reinterpret_cast<int32_t *>(rsm + wa);             // this rank's candidates
@@ -147,7 +150,7 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
             sh.pre[nr] = tot;
     }
     // this rank's positions [r_lo, r_hi) (r_lo a multiple of 32)
-    const int r_lo = min(L, rank * reuse_span(L)), r_hi = min(L, r_lo + reuse_span(L));
+    const int r_lo = min(L, rank * reuse_span(L, CL)), r_hi = min(L, r_lo + reuse_span(L, CL));
     const int nwords = (r_hi - r_lo + 31) >> 5;
     for (int i = tid; i < nwords; i += kReuseThreads)
         region[i] = 0u;
@@ -265,16 +268,16 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
     // every rank's list and count are complete, and every bitmap is dead (the
     // peers' scores may now land in the region that held it)
     cluster.sync();
-    if (tid < kReuseCluster)
+    if (tid < CL)
         sh.cpre[tid + 1] = *cluster.map_shared_rank(&sh.ncand, tid);
     __syncthreads();
     if (tid == 0) {
         sh.cpre[0] = 0;
-        for (int r = 0; r < kReuseCluster; ++r)
+        for (int r = 0; r < CL; ++r)
             sh.cpre[r + 1] += sh.cpre[r];
     }
     __syncthreads();
-    const int M = sh.cpre[kReuseCluster];
+    const int M = sh.cpre[CL];
     {   // A_t = the ranks' lists in rank order; four peer loads in flight
         for (int j0 = tid; j0 < M; j0 += 4 * kReuseThreads) {
             int32_t v[4];
@@ -285,7 +288,7 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
                 if (j < M) {
                     int r = 0;
 #pragma unroll
-                    for (int q = 1; q < kReuseCluster; ++q)
+                    for (int q = 1; q < CL; ++q)
                         r += j >= sh.cpre[q];
                     v[u] = cluster.map_shared_rank(loc, r)[j - sh.cpre[r]];
                 }
@@ -306,7 +309,7 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
     __syncthreads();
 
     // ---- Eq. (10): this rank's slice of the candidate scores -----------------
-    const int per = (M + kReuseCluster - 1) / kReuseCluster;
+    const int per = (M + CL - 1) / CL;
     const int cs = min(M, rank * per), ce = min(M, cs + per);
     {
         // half-warp hw scores rows jb + hw + 16u; the loop bound is the same for
@@ -347,7 +350,7 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
     }
     __syncthreads();   // the slice's scores are written
     // push the slice into every peer (each is past its bitmap: cluster barrier above)
-    for (int e = tid; e < (ce - cs) * (kReuseCluster - 1); e += kReuseThreads) {
+    for (int e = tid; e < (ce - cs) * (CL - 1); e += kReuseThreads) {
         const int p = e / (ce - cs), j = cs + e % (ce - cs);
         const int peer = p < rank ? p : p + 1;
         cluster.map_shared_rank(keys, peer)[j] = keys[j];
@@ -377,9 +380,9 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
     }
     __syncthreads();
     const float m = key2f(sh.kmax);
-    {   // S_t (identical in every rank), written 1/kReuseCluster per rank; every
+    {   // S_t (identical in every rank), written 1/CL per rank; every
         // rank of the cluster is past its reads of the retrieved supports
-        const int kper = (w.K + kReuseCluster - 1) / kReuseCluster;
+        const int kper = (w.K + CL - 1) / CL;
         const int j0 = rank * kper, j1 = min(w.K, j0 + kper);
         for (int jj = j0 + tid; jj < j1; jj += kReuseThreads) {
             const int32_t v = jj < n ? sup_i[jj] : -1;
@@ -394,7 +397,7 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
     }
 
     // ---- Eq. (12): this rank's share of the value rows -----------------------
-    const int vper = (n + kReuseCluster - 1) / kReuseCluster;
+    const int vper = (n + CL - 1) / CL;
     const int vs = min(n, rank * vper), ve = min(n, vs + vper);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float zsum = 0.f;
@@ -426,7 +429,7 @@ __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *sm
     if (tid < kD) {
         float o = 0.f, Z = 0.f;
 #pragma unroll
-        for (int r = 0; r < kReuseCluster; ++r) {
+        for (int r = 0; r < CL; ++r) {
             o += tl.part_o[r][tid];
             Z += tl.part_z[r];
         }

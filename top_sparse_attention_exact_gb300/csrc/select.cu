@@ -1,16 +1,18 @@
 // select.cu -- the exact path's select kernel for the stateless Exact Top-K
 // step and the cache initialisation (ReTopK paper, §Motivation Eq. (1),
-// §Recall-Before-Rerank Eq. (12)): one cluster of kExactCluster CTAs per
-// (sequence, query head) runs exact_select_body (select_body.cuh) after the
-// scan.  Decode steps run the same body inside the fused finish kernel.
+// §Recall-Before-Rerank Eq. (12)): one cluster of w.cluster CTAs (1, 2, 4 or
+// 8) per (sequence, query head) runs exact_select_body (select_body.cuh)
+// after the scan.  Decode steps run the same body inside the fused finish
+// kernel.
 #include "select_body.cuh"
 
 namespace retopk {
 
+template <int CL>
 __global__ void __launch_bounds__(kSelThreads, 2) exact_select_kernel(SelArgs a)
 {
     extern __shared__ __align__(128) unsigned char sel_smem[];
-    exact_select_body(a, sel_smem);
+    exact_select_body<CL>(a, sel_smem);
 }
 
 
@@ -30,17 +32,37 @@ cudaError_t launch_exact_select(const Work &w, QSrc q, const uint16_t *v_cache, 
     a.len_off = len_off;
     a.mode = mode;
     a.init_slot = init_slot;
-    return launch_pdl(exact_select_kernel, dim3(kExactCluster, w.B * w.Hq), dim3(kSelThreads), sel_smem_bytes(w.K), st, kExactCluster,
-                      a);
+    const dim3 grid(w.cluster, w.B * w.Hq), block(kSelThreads);
+    const size_t smem = sel_smem_bytes(w.K);
+    switch (w.cluster) {
+    case 1: return launch_pdl(exact_select_kernel<1>, grid, block, smem, st, 1, a);
+    case 2: return launch_pdl(exact_select_kernel<2>, grid, block, smem, st, 2, a);
+    case 4: return launch_pdl(exact_select_kernel<4>, grid, block, smem, st, 4, a);
+    case 8: return launch_pdl(exact_select_kernel<8>, grid, block, smem, st, 8, a);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int CL>
+static cudaError_t configure_one()
+{
+    cudaError_t e = cudaFuncSetAttribute(exact_select_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)sel_smem_bytes(kMaxK));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(exact_select_kernel<CL>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+    return e;
 }
 
 cudaError_t configure_select()
 {
-    cudaError_t e = cudaFuncSetAttribute(exact_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)sel_smem_bytes(kMaxK));
+    cudaError_t e = configure_one<1>();
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(exact_select_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared);
+        e = configure_one<2>();
+    if (e == cudaSuccess)
+        e = configure_one<4>();
+    if (e == cudaSuccess)
+        e = configure_one<8>();
     return e;
 }
 

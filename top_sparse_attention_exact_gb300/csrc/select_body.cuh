@@ -3,12 +3,14 @@
 // Eq. (12), and §Complexity and GPU Implementation: the paths differ only in
 // support discovery, so this back end mirrors the reuse kernel's).
 //
-// exact_select_kernel: one cluster of kExactCluster CTAs per exact-path
+// exact_select_kernel: one cluster of CL CTAs (CL = 1, 2, 4 or 8, at most
+// kExactCluster: chosen per configuration so that one wave of clusters covers
+// the heads) per exact-path
 // (sequence, query head), after the scan has written the head's fp32 scores
 // and its 11-bit score histogram.
 //   1. Every rank finds the threshold digit T1 -- the largest digit whose
 //      suffix count reaches min(K, L) -- from the histogram, and compacts the
-//      keys of its 1/kExactCluster slice whose digit is >= T1 (only they can
+//      keys of its 1/CL slice whose digit is >= T1 (only they can
 //      be in the Exact Top-K support), in ascending index order, into its own
 //      shared memory (up to kLocCap of them) and into its segment of the
 //      global candidate arrays.  The slice arrives in shared memory by one
@@ -25,7 +27,7 @@
 //      cluster barrier.  Every rank then runs the same radix select on
 //      (score, lower index first) and stable compaction: identical ascending
 //      supports in every rank.
-//   3. Each rank aggregates 1/kExactCluster of the support's V rows with the
+//   3. Each rank aggregates 1/CL of the support's V rows with the
 //      common max and pushes (weighted sum, sum of weights) to rank 0, which
 //      normalises, writes the output and -- on decode / init -- inserts
 //      (q_t, S_t) into the query-support cache (Eq. (5)).
@@ -186,13 +188,13 @@ static __device__ __noinline__ unsigned long long staged_refine(int N2, int rem,
 // place, in the global segments (offsets off[] of the unfiltered per-rank
 // lists), compact the support into sup_i / sup_k and leave its maximum key in
 // kmax.  Returns the support's length.
-static __device__ __noinline__ int global_select(int N, int need, int K, int seg, const int *off, const int32_t *gi,
-                                          const uint32_t *gk, int32_t *sup_i, uint32_t *sup_k, SelectShared &sel,
-                                          uint32_t *kmax)
+static __device__ __noinline__ int global_select(int N, int need, int K, int seg, int ranks, const int *off,
+                                                 const int32_t *gi, const uint32_t *gk, int32_t *sup_i,
+                                                 uint32_t *sup_k, SelectShared &sel, uint32_t *kmax)
 {
     auto get = [&](int j, int32_t &idx, uint32_t &k) {
         int r = 0;
-        while (r + 1 < kExactCluster && off[r + 1] <= j)
+        while (r + 1 < ranks && off[r + 1] <= j)
             ++r;
         const int o = r * seg + (j - off[r]);
         idx = gi[o];
@@ -210,10 +212,12 @@ static __device__ __noinline__ int global_select(int N, int need, int K, int seg
     return n;
 }
 
-// One exact-path head per cluster of kExactCluster CTAs of kSelThreads
-// threads; `smem` is the CTA's dynamic shared memory (sel_smem_bytes).
+// One exact-path head per cluster of CL CTAs of kSelThreads threads; `smem`
+// is the CTA's dynamic shared memory (sel_smem_bytes).
+template <int CL>
 __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned char *smem)
 {
+    static_assert(CL == 1 || CL == 2 || CL == 4 || CL == 8, "cluster of 1, 2, 4 or 8 CTAs");
     SelShared &sh = *reinterpret_cast<SelShared *>(smem);
     unsigned char *xs = smem + kSelSharedBytes;
     cg::cluster_group cluster = cg::this_cluster();
@@ -236,7 +240,7 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     }
     const int L = seq_len(a.seqlens, b, a.len_off, w.max_len);
     const int need = min(w.K, L);
-    const int seg = (((L + kExactCluster - 1) / kExactCluster) + 15) & ~15;
+    const int seg = (((L + CL - 1) / CL) + 15) & ~15;
     const int start = min(L, rank * seg), end = min(L, start + seg);
     const float *sc = w.scores + (size_t)bh * w.sc_stride;
     int32_t *oi = w.cand_idx + (size_t)bh * w.cand_stride + (size_t)rank * seg;
@@ -383,13 +387,14 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
         count += total;
         __syncthreads();                                  // before the next chunk overwrites the slice
     }
-    if (tid < kExactCluster)
+    if (tid < CL)
         cluster.map_shared_rank(&sh.cnt[0], tid)[rank] = count;
     {   // this rank's second-level histogram to every rank: one uint4 per thread
         static_assert(kExactCluster * kSubBins / 4 == kSelThreads, "push layout");
         const int r = tid / (kSubBins / 4), q4 = tid % (kSubBins / 4);
-        reinterpret_cast<uint4 *>(cluster.map_shared_rank(&sh.h2all[rank][0], r))[q4] =
-            reinterpret_cast<const uint4 *>(sh.h2)[q4];
+        if (r < CL)
+            reinterpret_cast<uint4 *>(cluster.map_shared_rank(&sh.h2all[rank][0], r))[q4] =
+                reinterpret_cast<const uint4 *>(sh.h2)[q4];
     }
     cluster.sync();   // every rank's candidates (shared and global), count and histogram are visible
 
@@ -400,13 +405,13 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     // selected.  Thread t (< kSubBins) takes bin kSubBins - 1 - t.
     int N = 0;
 #pragma unroll
-    for (int r = 0; r < kExactCluster; ++r)
+    for (int r = 0; r < CL; ++r)
         N += sh.cnt[r];
     {
         uint32_t hsum = 0u;
         if (tid < kSubBins) {
 #pragma unroll
-            for (int r = 0; r < kExactCluster; ++r)
+            for (int r = 0; r < CL; ++r)
                 hsum += sh.h2all[r][kSubBins - 1 - tid];
         }
         int tot;
@@ -421,7 +426,7 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     const uint32_t p19 = ((uint32_t)T1 << 8) | (uint32_t)sh.T2;
     // final candidates per rank: its keys above digit T1 plus its digit-T1 keys
     // whose second-level digit is >= T2 (warp r counts rank r)
-    if (warp < kExactCluster) {
+    if (warp < CL) {
         int all = 0, ge = 0;
 #pragma unroll
         for (int i = 0; i < kSubBins / 32; ++i) {
@@ -438,14 +443,14 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     __syncthreads();
     if (tid == 0) {
         int acc = 0;
-        for (int r = 0; r < kExactCluster; ++r) {
+        for (int r = 0; r < CL; ++r) {
             sh.off[r] = acc;
             acc += sh.wcnt[r];
         }
-        sh.off[kExactCluster] = acc;
+        sh.off[CL] = acc;
     }
     __syncthreads();
-    const int N2 = sh.off[kExactCluster];
+    const int N2 = sh.off[CL];
     const int32_t *gi = w.cand_idx + (size_t)bh * w.cand_stride;
     const uint32_t *gk = w.cand_key + (size_t)bh * w.cand_stride;
     const bool staged = N2 <= kSelStageCap;
@@ -454,10 +459,10 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     // histories): each rank pushes its own, compacted by all its threads.
     int cmax = 0;
 #pragma unroll
-    for (int r = 0; r < kExactCluster; ++r)
+    for (int r = 0; r < CL; ++r)
         cmax = max(cmax, sh.cnt[r]);
     const bool push = cmax > kLocCap;
-    if (staged && !push && warp < kExactCluster) {
+    if (staged && !push && warp < CL) {
         // warp r gathers rank r's final candidates in order from its shared memory
         const int r = warp, cr = sh.cnt[r];
         const int32_t *pi = cluster.map_shared_rank(loc_i, r);
@@ -522,7 +527,7 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
                 if (j0 + u < cr && (kk[u] >> kSub) >= p19) {
                     if (d < o1) {   // the histogram's count bounds the rank's range
 #pragma unroll
-                        for (int r2 = 0; r2 < kExactCluster; ++r2) {
+                        for (int r2 = 0; r2 < CL; ++r2) {
                             cluster.map_shared_rank(st_idx, r2)[d] = ii[u];
                             cluster.map_shared_rank(st_key, r2)[d] = kk[u];
                         }
@@ -590,19 +595,19 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
         // in place, in global memory (offsets of the unfiltered segments)
         if (tid == 0) {
             int acc = 0;
-            for (int r = 0; r < kExactCluster; ++r) {
+            for (int r = 0; r < CL; ++r) {
                 sh.off[r] = acc;
                 acc += sh.cnt[r];
             }
-            sh.off[kExactCluster] = acc;
+            sh.off[CL] = acc;
         }
         __syncthreads();
-        n = global_select(N, need, w.K, seg, sh.off, gi, gk, sup_i, sup_k, sh.sel, &sh.kmax);
+        n = global_select(N, need, w.K, seg, CL, sh.off, gi, gk, sup_i, sup_k, sh.sel, &sh.kmax);
     }
     __syncthreads();
     const float m = key2f(sh.kmax);
-    {   // the support (identical in every rank), written 1/kExactCluster per rank
-        const int kper = (w.K + kExactCluster - 1) / kExactCluster;
+    {   // the support (identical in every rank), written 1/CL per rank
+        const int kper = (w.K + CL - 1) / CL;
         const int j0 = rank * kper, j1 = min(w.K, j0 + kper);
         for (int jj = j0 + tid; jj < j1; jj += kSelThreads) {
             const int32_t v = jj < n ? sup_i[jj] : -1;
@@ -629,7 +634,7 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float zsum = 0.f;
     if (a.mode != FIN_INIT) {   // cache initialisation needs the support only
-        const int vper = (n + kExactCluster - 1) / kExactCluster;
+        const int vper = (n + CL - 1) / CL;
         const int vs = min(n, rank * vper), ve = min(n, vs + vper);
         value_partial<8>(vb, sup_i, sup_k, vs + warp, ve, kSelWarps, m, acc, zsum, L, w.status);
     }
@@ -659,7 +664,7 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     if (tid < kD) {
         float o = 0.f, Z = 0.f;
 #pragma unroll
-        for (int r = 0; r < kExactCluster; ++r) {
+        for (int r = 0; r < CL; ++r) {
             o += sh.part_o[r][tid];
             Z += sh.part_z[r];
         }

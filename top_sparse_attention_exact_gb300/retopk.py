@@ -43,7 +43,7 @@ class retopk_config(ctypes.Structure):
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("max_len", ctypes.c_int32), ("K", ctypes.c_int32), ("C", ctypes.c_int32),
                 ("W", ctypes.c_int32), ("R", ctypes.c_int32), ("T_r", ctypes.c_int32),
-                ("tau", ctypes.c_float), ("retrieval", ctypes.c_int32)]
+                ("tau", ctypes.c_float), ("retrieval", ctypes.c_int32), ("cluster", ctypes.c_int32)]
 
 
 _P, _S, _I = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
@@ -264,10 +264,10 @@ class ReTopK:
     """A ReTopK decode context (query-support cache + scratch in a torch buffer)."""
 
     def __init__(self, B, Hq, Hkv, max_len, K=512, C=32, W=32, R=4, T_r=128, tau=0.85, d=128,
-                 device="cuda", recent: bool = False, scratch: torch.Tensor | None = None):
+                 device="cuda", recent: bool = False, scratch: torch.Tensor | None = None, cluster: int = 0):
         """scratch: optional uint8 CUDA tensor of at least scratch_bytes(...) + 256 bytes, shared with
         other contexts whose steps run one after another on one stream (retopk_create_shared)."""
-        self.cfg = retopk_config(B, Hq, Hkv, d, max_len, K, C, W, R, T_r, tau, 1 if recent else 0)
+        self.cfg = retopk_config(B, Hq, Hkv, d, max_len, K, C, W, R, T_r, tau, 1 if recent else 0, cluster)
         lib = load()
         h = ctypes.c_void_p()
         if scratch is None:

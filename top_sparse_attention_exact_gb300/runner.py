@@ -27,7 +27,7 @@ class DecodeRun:
     scratch with other contexts (retopk_create_shared)."""
 
     def __init__(self, w: synth.Workload, arrays=None, device="cuda", max_len=None, fused: bool = True,
-                 scratch=None):
+                 scratch=None, cluster: int = 0):
         self.w = w
         self.fused = fused
         self.device = torch.device(device)
@@ -47,7 +47,7 @@ class DecodeRun:
         self.v_new = to_dev(np.ascontiguousarray(v[:, :, L0:].transpose(2, 0, 1, 3)), dev)
         self.out = torch.zeros((B, w.Hq, d), dtype=torch.int16, device=dev)
         self.ctx = ReTopK(B, w.Hq, Hkv, self.max_len, K=w.K, C=w.C, W=w.W, R=w.R, T_r=w.T_r,
-                          tau=w.tau, d=d, device=dev, recent=w.recent, scratch=scratch)
+                          tau=w.tau, d=d, device=dev, recent=w.recent, scratch=scratch, cluster=cluster)
         self.ctx.retopk_init_cache(self.q_prompt, self.k_cache, self.seqlens)
         self.t = 0
         self.graph = None
