@@ -76,12 +76,13 @@ enum {
  * Limits: d = 128; 1 <= Hq/Hkv <= 16; B * Hkv <= 512; 1 <= K <= 4096;
  * 1 <= R <= C <= 256; 0 <= W; R*K + W <= 18432; max_len <= 2^23 and
  * B * Hkv * max_len <= 2^29; B * Hq * C * K < 2^31.  The reuse path keeps, per
- * CTA of a head's cluster of 8, a bitmap over max_len/8 key positions and
+ * CTA of a head's cluster of CL (`cluster`; 8 when chosen automatically and
+ * the smaller sizes do not fit), a bitmap over max_len/CL key positions and
  * three lists of R*K + W words in shared memory, which must fit 227 KB:
- * 5376 + 4 * (max(ceil(max_len/8)/32, R*K + W) + max(R*K + W, 3096) + R*K + W)
- * bytes, each count of words rounded up to 32 positions or 4 words (e.g.
- * max_len = 2^23 with R*K + W = 2080, or R*K + W = 18432 with max_len <=
- * 5095424).  Larger combinations return RETOPK_ERR_UNSUPPORTED. */
+ * 5376 + 4 * (max(ceil(max_len/CL)/32, R*K + W) + max(R*K + W, 3096) + R*K + W)
+ * bytes, each count of words rounded up to 32 positions or 4 words (e.g., at
+ * CL = 8, max_len = 2^23 with R*K + W = 2080, or R*K + W = 18432 with
+ * max_len <= 5095424).  Larger combinations return RETOPK_ERR_UNSUPPORTED. */
 typedef struct retopk_config {
     int32_t batch;        /* B                                                  */
     int32_t n_q_heads;    /* Hq                                                 */
