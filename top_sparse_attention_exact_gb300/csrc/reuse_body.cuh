@@ -38,7 +38,6 @@ namespace cg = cooperative_groups;
 constexpr int kReuseThreads = 512;
 constexpr int kReuseWarps = kReuseThreads / 32;
 constexpr int kReuseCluster = 8;
-constexpr int kRerankRows = 4;        // key rows in flight per half-warp
 static_assert(kMaxC <= kReuseThreads, "one cache entry per thread");
 
 struct ReuseArgs {
@@ -105,6 +104,9 @@ template <int CL>
 __device__ __forceinline__ void reuse_body(const ReuseArgs &a, unsigned char *smem)
 {
     static_assert(CL == 1 || CL == 2 || CL == 4 || CL == 8, "cluster of 1, 2, 4 or 8 CTAs");
+    // key rows in flight per half-warp: twice as many when one or two CTAs
+    // carry the head (large batches, where the candidates per CTA are many)
+    constexpr int kRerankRows = CL <= 2 ? 8 : 4;
     ReuseShared &sh = *reinterpret_cast<ReuseShared *>(smem);
     uint32_t *rsm = reinterpret_cast<uint32_t *>(smem + kReuseSharedBytes);
     cg::cluster_group cluster = cg::this_cluster();
