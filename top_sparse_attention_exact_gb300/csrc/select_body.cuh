@@ -49,7 +49,10 @@ namespace retopk {
 
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kSliceCap = 17408;                   // scores per bulk copy (68 KiB): one copy per rank up to 136K keys
+// scores per bulk copy (67.5 KiB): one copy per rank up to 138K keys, and two
+// CTAs of the select (sel_smem_bytes, 115,712 bytes at K = 2048) per 228 KB SM
+// up to K = 2048
+constexpr int kSliceCap = 17280;
 constexpr int kSelStageCap = 8192;                 // candidates staged in shared memory
 constexpr int kLocCap = 1024;                      // candidates a rank keeps in its own shared memory
 constexpr int kBlkGroups = 32;                     // filter block: 32 groups of four scores
