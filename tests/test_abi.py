@@ -43,6 +43,8 @@ def test_config_validation_without_gpu(lib):
     ok = retopk.retopk_config(1, 28, 4, 128, 131584, 512, 32, 32, 4, 128, 0.85)
     assert lib.retopk_workspace_bytes(ctypes.byref(ok)) > 0
     for good in (retopk.retopk_config(1, 28, 4, 128, 1 << 23, 512, 32, 32, 4, 128, 0.85),
+                 retopk.retopk_config(16, 28, 4, 128, 65792, 2048, 32, 32, 4, 128, 0.85, 0, 1),
+                 retopk.retopk_config(1, 28, 4, 128, 131584, 512, 32, 32, 4, 128, 0.85, 0, 2),
                  retopk.retopk_config(1, 28, 4, 128, 5095424, 4096, 8, 2048, 4, 128, 0.85)):
         assert lib.retopk_workspace_bytes(ctypes.byref(good)) > 0
     bad = [
@@ -59,6 +61,10 @@ def test_config_validation_without_gpu(lib):
         retopk.retopk_config(1, 28, 4, 128, 5095424 + 1, 4096, 8, 2048, 4, 128, 0.85),
         retopk.retopk_config(1, 28, 4, 128, 1024, 512, 32, 32, 4, 128, float("nan")),
         retopk.retopk_config(1, 28, 4, 128, 1024, 512, 32, 32, 4, 128, 0.85, 2),   # retrieval mode
+        retopk.retopk_config(1, 28, 4, 128, 1024, 512, 32, 32, 4, 128, 0.85, 0, 3),   # cluster size
+        retopk.retopk_config(1, 28, 4, 128, 1024, 512, 32, 32, 4, 128, 0.85, 0, 16),
+        # a fixed cluster of one CTA: the bitmap over all of max_len no longer fits
+        retopk.retopk_config(1, 28, 4, 128, 1 << 23, 512, 32, 32, 4, 128, 0.85, 0, 1),
     ]
     for c in bad:
         assert lib.retopk_workspace_bytes(ctypes.byref(c)) == 0
