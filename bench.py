@@ -351,13 +351,14 @@ def layers_pass(w, arrays, dev, n_layers, n_tokens, warm, flush, stream):
                    "query-support state sharing one per-step scratch (retopk_create_shared), same inputs"}
 
 
-def scan_roofline(w, dr, ex, t_mid, flush, stream, n_launch=8, reps=12):
+def scan_roofline(w, dr, ex, t_mid, flush, stream, n_launch=32, reps=12):
     """The full-history scan's own launch duration: one CUDA graph of n_launch
     back-to-back exact_topk_scan calls (histogram clear + scan: the exact step's
     first half) alternating between two copies of the K cache (each larger
     than the L2; the L2 is also flushed before every replay), CUDA events around
     each replay; per-launch time = replay time / n_launch (it includes the
-    clear kernel and the launch gaps).  Query and length of decode step t_mid."""
+    clear kernel and the launch gaps, and 1/n_launch of the replay's own
+    launch and completion).  Query and length of decode step t_mid."""
     import torch
     from top_sparse_attention_exact_gb300 import retopk
     k2 = dr.k_cache.clone()
