@@ -219,6 +219,17 @@ def test_largest_max_len_short_history():
     assert (np.concatenate(paths) == 0).sum() >= 4
 
 
+def test_qwen_1m_prefilter_sampled():
+    # 1M keys, 28 heads: a CTA's eighth of an exact head's scores spans
+    # several windows, so decode steps run the exact-head prefilter; mixed
+    # steps and the refresh at step 128 (every head exact) against the oracle
+    w = synth.scaled(synth.WORKLOADS["qwen7b_1m"], steps=130, name="qwen7b_1m_pf")
+    dr, errs, agg, paths = run_checked(w, check_steps={1, 2, 3, 4, 5, 6, 127, 128, 129, 130})
+    assert not errs, "\n".join(errs[:20])
+    p = np.concatenate(paths)
+    assert ((p != 0).sum() > 0) and (p[-3 * w.Hq:-2 * w.Hq] == 2).all()
+
+
 def test_long_history_split_bitmap():
     # 3M keys: each rank's bitmap slice covers ~393K positions and the
     # retrieved supports spread over all of them

@@ -17,6 +17,7 @@ cudaError_t configure_select();
 cudaError_t configure_finish();
 size_t finish_smem_bytes_for(int max_len, int K, int RKW, int CL);
 cudaError_t configure_fidelity();
+cudaError_t configure_prefilter();
 }  // namespace retopk
 
 using namespace retopk;
@@ -113,6 +114,8 @@ int ensure_configured()
             e = configure_finish();
         if (e == cudaSuccess)
             e = configure_fidelity();
+        if (e == cudaSuccess)
+            e = configure_prefilter();
         err[dev] = e;
     });
     return cuda_rc(err[dev]);
@@ -201,12 +204,22 @@ size_t plan_scratch(const retopk_config &c, bool stateful, Work *w, char *base)
     const size_t o_ck = L.add(BH * cand_stride * 4);
     const size_t o_sc = L.add(BH * (size_t)sc_stride * 4);
     const size_t o_h = L.add(BH * kHistBins * 4);
+    // the exact-head prefilter's arrays (decode contexts whose CTAs at 8 per
+    // head hold more than one window of scores)
+    const int seg8 = (((c.max_len + kExactCluster - 1) / kExactCluster) + 15) & ~15;
+    const int pf_nw = stateful && seg8 > kSliceCap ? (seg8 + kSliceCap - 1) / kSliceCap : 0;
+    size_t o_pfc = 0, o_pfh = 0;
+    if (pf_nw) {
+        o_pfc = L.add(BH * kExactCluster * pf_nw * 4);
+        o_pfh = L.add(BH * kExactCluster * 256 * 4);
+    }
     const size_t o_sup = L.add(BH * c.K * 4);
     const size_t o_sl = L.add(BH * 4);
     const size_t o_of = L.add(BH * kD * 4);
     if (w) {
         w->cand_stride = cand_stride;
         w->sc_stride = sc_stride;
+        w->pf_nw = pf_nw;
     }
     if (base && w) {
         if (stateful) {
@@ -222,6 +235,8 @@ size_t plan_scratch(const retopk_config &c, bool stateful, Work *w, char *base)
         w->cand_idx = (int32_t *)(base + o_ci);
         w->cand_key = (uint32_t *)(base + o_ck);
         w->scores = (float *)(base + o_sc);
+        w->pf_cnt = pf_nw ? (int32_t *)(base + o_pfc) : nullptr;
+        w->pf_h2 = pf_nw ? (uint32_t *)(base + o_pfh) : nullptr;
         w->hist = (uint32_t *)(base + o_h);
         w->support = (int32_t *)(base + o_sup);
         w->sup_len = (int32_t *)(base + o_sl);
@@ -449,6 +464,7 @@ int retopk_create_shared(const retopk_config *cfg, void *d_state, size_t state_b
     plan_scratch(*cfg, true, &c->w, (char *)d_scratch);
     c->w.n_scan = n_scan_for(cfg->batch, cfg->n_kv_heads, cfg->max_len);
     c->w.cluster = cluster_for(*cfg, true);
+    c->w.prefilter = c->w.pf_nw > 0 && c->w.cluster == kExactCluster && (long long)cfg->batch * cfg->n_q_heads <= kPfMaxHeads;
     // the state starts at zero; the scratch holds nothing a step reads before writing it
     cudaError_t ce = cudaMemset(d_state, 0, ns);
     if (ce == cudaSuccess)
@@ -482,6 +498,7 @@ int retopk_create(const retopk_config *cfg, void *d_workspace, size_t bytes, ret
     plan(*cfg, true, &c->w, (char *)d_workspace);
     c->w.n_scan = n_scan_for(cfg->batch, cfg->n_kv_heads, cfg->max_len);
     c->w.cluster = cluster_for(*cfg, true);
+    c->w.prefilter = c->w.pf_nw > 0 && c->w.cluster == kExactCluster && (long long)cfg->batch * cfg->n_q_heads <= kPfMaxHeads;
     cudaError_t ce = cudaMemset(d_workspace, 0, plan(*cfg, true, nullptr, nullptr));
     if (ce == cudaSuccess)
         ce = cudaDeviceSynchronize();
@@ -585,6 +602,8 @@ int decode_step(retopk_ctx *ctx, const retopk_bf16 *k_new, const retopk_bf16 *v_
          }))))
         return e;
     if ((e = run_scan(w, qs, k_cache, d_seqlens, 0, st)))
+        return e;
+    if (w.prefilter && (e = cuda_rc(launch_prefilter(w, d_seqlens, st))))
         return e;
     return cuda_rc(timed(RETOPK_PROF_FINISH, st,
                          [&] { return launch_finish(w, qk, k_cache, v_cache, d_seqlens, out, st); }));

@@ -21,6 +21,11 @@ constexpr int kMaxC = 256;
 constexpr int kExactCluster = 8;    // CTAs (candidate segments) per exact-path head
 constexpr int kMaxSeqGroups = 512;  // B * Hkv handled by one scan launch
 constexpr int kMaxCand = 18432;     // R*K + W (the candidate lists live in smem)
+// scores per window of the exact select (67.5 KiB): one window per CTA up to
+// 138K keys at 8 CTAs per head, and two CTAs of the select (115,712 bytes of
+// shared memory at K = 2048) per 228 KB SM up to K = 2048
+constexpr int kSliceCap = 17280;
+constexpr int kPfMaxHeads = 64;     // decode steps with the exact-head prefilter: at most this many heads
 constexpr size_t kMaxDynSmem = 227 * 1024;   // dynamic shared memory of one CTA
 
 // Per-sequence control words.
@@ -55,6 +60,14 @@ struct Work {
     int32_t *cand_idx;   // [B*Hq*cand_stride]
     uint32_t *cand_key;  // [B*Hq*cand_stride]
     float *scores;       // [B*Hq*sc_stride]
+    // Exact-head prefilter of long-history decode steps (8 CTAs per head, a
+    // CTA's share of the scores longer than one window, at most kPfMaxHeads
+    // heads): per (head, rank, window) its first-digit candidate count, and
+    // per (head, rank) the second-digit histogram of its digit-T1 keys
+    int prefilter;       // decode steps run it
+    int pf_nw;           // windows per rank at max_len (0: no arrays)
+    int32_t *pf_cnt;     // [B*Hq*kExactCluster*pf_nw]
+    uint32_t *pf_h2;     // [B*Hq*kExactCluster*256], cleared with the histogram
     uint32_t *hist;      // [B*Hq*kHistBins]
     int32_t *support;    // [B*Hq*K]
     int32_t *sup_len;    // [B*Hq]
@@ -253,6 +266,7 @@ cudaError_t launch_append(const Work &w, const uint16_t *k_new, const uint16_t *
                           uint16_t *k_cache, uint16_t *v_cache, int32_t *seqlens, cudaStream_t st);
 cudaError_t launch_init_done(const Work &w, cudaStream_t st);
 cudaError_t launch_clear_words(void *p, size_t bytes, cudaStream_t st);
+cudaError_t launch_prefilter(const Work &w, const int32_t *seqlens, cudaStream_t st);
 cudaError_t launch_selftest_wait(uint32_t *status, long long limit, cudaStream_t st);
 int scan_ctas_per_sm();
 

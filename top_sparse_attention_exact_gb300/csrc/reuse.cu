@@ -156,6 +156,11 @@ __global__ void __launch_bounds__(kDecideThreads) decide_kernel(DecideArgs a)
         uint4 *hg = reinterpret_cast<uint4 *>(w.hist + (size_t)bh * kHistBins);
         for (int i = tid; i < kHistBins / 4; i += kDecideThreads)
             hg[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (w.prefilter) {          // and for the prefilter's second-digit histograms
+            uint4 *h2 = reinterpret_cast<uint4 *>(w.pf_h2 + (size_t)bh * kExactCluster * 256);
+            for (int i = tid; i < kExactCluster * 256 / 4; i += kDecideThreads)
+                h2[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
     }
 }
 

@@ -49,10 +49,6 @@ namespace retopk {
 
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
-// scores per bulk copy (67.5 KiB): one copy per rank up to 138K keys, and two
-// CTAs of the select (sel_smem_bytes, 115,712 bytes at K = 2048) per 228 KB SM
-// up to K = 2048
-constexpr int kSliceCap = 17280;
 constexpr int kSelStageCap = 8192;                 // candidates staged in shared memory
 constexpr int kLocCap = 1024;                      // candidates a rank keeps in its own shared memory
 constexpr int kBlkGroups = 32;                     // filter block: 32 groups of four scores
@@ -215,6 +211,56 @@ static __device__ __noinline__ int global_select(int N, int need, int K, int seg
     return n;
 }
 
+// Long-history decode steps: the exact-head prefilter (prefilter.cu) has
+// listed this rank's first-digit candidates window by window -- window v's
+// count in pf_cnt, its candidates at offset v * kSliceCap of the rank's global
+// segment -- and their second-digit histogram in pf_h2.  Compacts the lists
+// in place, window by window (a window's destinations start no later than
+// its sources, so a chunk read in full before it is written never clobbers
+// unread entries), the first kLocCap also into shared memory, and loads the
+// histogram into sh.h2.  Returns the rank's count.
+static __device__ __noinline__ int gather_prefiltered(const Work &w, int bh, int rank, int range, int32_t *loc_i,
+                                                      uint32_t *loc_k, int32_t *oi, uint32_t *ok, SelShared &sh)
+{
+    const int tid = threadIdx.x;
+    const int nw = (range + kSliceCap - 1) / kSliceCap;   // <= pf_nw <= kMaxBlk
+    const int32_t *pc = w.pf_cnt + ((size_t)bh * kExactCluster + rank) * w.pf_nw;
+    const int cv = tid < nw ? pc[tid] : 0;
+    int total;
+    const int pre = block_excl_scan<kSelThreads>(cv, sh.sel.warp_tot, total);
+    if (tid < nw) {
+        sh.bcnt[tid] = cv;
+        sh.boff[tid] = pre;
+    }
+    if (tid < kSubBins)
+        sh.h2[tid] = w.pf_h2[((size_t)bh * kExactCluster + rank) * kSubBins + tid];
+    __syncthreads();
+    for (int v = 0; v < nw; ++v) {                    // uniform trip counts
+        const int c = sh.bcnt[v], d0 = sh.boff[v], s0 = v * kSliceCap;
+        for (int j0 = 0; j0 < c; j0 += kSelThreads) {
+            const int j = j0 + tid;
+            int32_t ix = 0;
+            uint32_t k = 0u;
+            if (j < c) {
+                ix = oi[s0 + j];
+                k = ok[s0 + j];
+            }
+            __syncthreads();
+            if (j < c) {
+                const int p = d0 + j;
+                if (p < kLocCap) {
+                    loc_i[p] = ix;
+                    loc_k[p] = k;
+                }
+                oi[p] = ix;
+                ok[p] = k;
+            }
+            __syncthreads();
+        }
+    }
+    return total;
+}
+
 // One exact-path head per cluster of CL CTAs of kSelThreads threads; `smem`
 // is the CTA's dynamic shared memory (sel_smem_bytes).
 template <int CL>
@@ -285,7 +331,11 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
         if (tid < n - nb)
             slice[nb + tid] = sc[c0 + nb + tid];
     };
-    issue(start, min(end - start, kSliceCap));
+    // decode steps of long histories: the prefilter kernel has listed this
+    // rank's first-digit candidates window by window
+    const bool prefiltered = a.mode == FIN_DECODE && w.prefilter;
+    if (!prefiltered)
+        issue(start, min(end - start, kSliceCap));
     const uint4 hv = reinterpret_cast<const uint4 *>(w.hist + (size_t)bh * kHistBins)[tid];   // digits [4t, 4t+4)
     {
         const int part = (int)(hv.x + hv.y + hv.z + hv.w);
@@ -311,7 +361,9 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     const uint32_t tcmp = tkey >= 0x80000000u ? (tkey & 0x7fffffffu) : ~tkey;
     int count = 0;
     uint32_t parity = 0;
-    for (int c0 = start; c0 < end; c0 += kSliceCap) {   // uniform trip count
+    if (prefiltered)
+        count = gather_prefiltered(w, bh, rank, end - start, loc_i, loc_k, oi, ok, sh);
+    for (int c0 = start; c0 < end && !prefiltered; c0 += kSliceCap) {   // uniform trip count
         const int n = min(end - c0, kSliceCap);
         if (c0 != start)
             issue(c0, n);
