@@ -65,6 +65,8 @@ constexpr size_t kSelRegionBytes = (size_t)kSliceCap * 4 > (size_t)kSelStageCap 
 // arrays are dead
 static_assert((size_t)kSelWarps * kD * 4 <= kSelRegionBytes, "value partials fit the region");
 static_assert(kHistBins == 4 * kSelThreads, "one uint4 of histogram per thread");
+constexpr int kMaxTie = 128;                       // tied keys one warp ranks (four per lane)
+static_assert(kMaxBlk * kBlkGroups >= kMaxTie * 8, "the tie list fits the filter masks");
 
 struct SelArgs {
     Work w;
@@ -81,7 +83,9 @@ struct SelShared {
     uint64_t bar;                                  // bulk-copy completion (score slices)
     int T1, T2, above2;
     int wcnt[kSelWarps];                           // final candidates per rank (phase 2)
-    uint8_t gmask[kMaxBlk * kBlkGroups];           // filter: bit e of group g = score 4g + e passes
+    // filter: bit e of group g = score 4g + e passes; in phase 2 the tied
+    // keys' composite keys (tie list, at most kMaxTie)
+    alignas(16) uint8_t gmask[kMaxBlk * kBlkGroups];
     int bcnt[kMaxBlk], boff[kMaxBlk];              // candidates per block, and their first position
     int cnt[kExactCluster];                        // candidates per rank
     int off[kExactCluster + 1];                    // final candidates: offsets per rank
@@ -89,7 +93,6 @@ struct SelShared {
     alignas(16) uint32_t h2all[kExactCluster][kSubBins];   // every rank's h2 (pushed by the ranks)
     SelectShared sel;
     int ntie;                                      // final candidates sharing the prefix (T1, T2)
-    unsigned long long tie[32];                    // their composite keys (when at most 32)
     unsigned long long tie_thr;                    // the rem-th largest of them
     uint32_t kmax;
     float zw[kSelWarps];
@@ -215,48 +218,62 @@ static __device__ __noinline__ int global_select(int N, int need, int K, int seg
 // listed this rank's first-digit candidates window by window -- window v's
 // count in pf_cnt, its candidates at offset v * kSliceCap of the rank's global
 // segment -- and their second-digit histogram in pf_h2.  Compacts the lists
-// in place, window by window (a window's destinations start no later than
-// its sources, so a chunk read in full before it is written never clobbers
-// unread entries), the first kLocCap also into shared memory, and loads the
-// histogram into sh.h2.  Returns the rank's count.
+// in place into positions 0 .. count-1 (the first kLocCap also into shared
+// memory) and loads the histogram into sh.h2.  Entry j of the compacted list
+// comes from position >= j, so batches of kSelThreads * 4 entries, each read
+// in full (every load of a batch in flight at once) before it is written, in
+// order, never clobber an entry not yet read.  Returns the rank's count.
 static __device__ __noinline__ int gather_prefiltered(const Work &w, int bh, int rank, int range, int32_t *loc_i,
                                                       uint32_t *loc_k, int32_t *oi, uint32_t *ok, SelShared &sh)
 {
+    constexpr int kPer = 4;
     const int tid = threadIdx.x;
     const int nw = (range + kSliceCap - 1) / kSliceCap;   // <= pf_nw <= kMaxBlk
     const int32_t *pc = w.pf_cnt + ((size_t)bh * kExactCluster + rank) * w.pf_nw;
     const int cv = tid < nw ? pc[tid] : 0;
     int total;
     const int pre = block_excl_scan<kSelThreads>(cv, sh.sel.warp_tot, total);
-    if (tid < nw) {
-        sh.bcnt[tid] = cv;
+    if (tid < nw)
         sh.boff[tid] = pre;
-    }
     if (tid < kSubBins)
         sh.h2[tid] = w.pf_h2[((size_t)bh * kExactCluster + rank) * kSubBins + tid];
     __syncthreads();
-    for (int v = 0; v < nw; ++v) {                    // uniform trip counts
-        const int c = sh.bcnt[v], d0 = sh.boff[v], s0 = v * kSliceCap;
-        for (int j0 = 0; j0 < c; j0 += kSelThreads) {
-            const int j = j0 + tid;
-            int32_t ix = 0;
-            uint32_t k = 0u;
-            if (j < c) {
-                ix = oi[s0 + j];
-                k = ok[s0 + j];
-            }
-            __syncthreads();
-            if (j < c) {
-                const int p = d0 + j;
-                if (p < kLocCap) {
-                    loc_i[p] = ix;
-                    loc_k[p] = k;
+    for (int j0 = 0; j0 < total; j0 += kSelThreads * kPer) {   // uniform trip count
+        int32_t ix[kPer];
+        uint32_t k[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int j = j0 + u * kSelThreads + tid;
+            ix[u] = 0;
+            k[u] = 0u;
+            if (j < total) {
+                int lo = 0, hi = nw - 1;   // the window holding entry j: last v with boff[v] <= j
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (sh.boff[mid] <= j)
+                        lo = mid;
+                    else
+                        hi = mid - 1;
                 }
-                oi[p] = ix;
-                ok[p] = k;
+                const int src = lo * kSliceCap + (j - sh.boff[lo]);
+                ix[u] = oi[src];
+                k[u] = ok[src];
             }
-            __syncthreads();
         }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int j = j0 + u * kSelThreads + tid;
+            if (j < total) {
+                if (j < kLocCap) {
+                    loc_i[j] = ix[u];
+                    loc_k[j] = k[u];
+                }
+                oi[j] = ix[u];
+                ok[j] = k[u];
+            }
+        }
+        __syncthreads();
     }
     return total;
 }
@@ -612,38 +629,43 @@ __device__ __forceinline__ void exact_select_body(const SelArgs &a, unsigned cha
     unsigned long long thr = 0ull;
     if (staged) {
         // every key above prefix (T1, T2) is in; the need - above2 others come
-        // from the keys with that prefix.  Those few are listed and ranked by
-        // one warp (composite keys are distinct); more than 32 of them take the
+        // from the keys with that prefix.  Those few are listed (in the filter
+        // masks' space, dead by now) and ranked by one warp, four per lane
+        // (composite keys are distinct); more than kMaxTie of them take the
         // radix refinement, and a histogram that disagreed with the scores (no
         // T2 found) falls back to the full select.
         const int rem = need - sh.above2;
+        unsigned long long *tie = reinterpret_cast<unsigned long long *>(sh.gmask);
         if (N2 > need && sh.above2 >= 0) {
             for (int j = tid; j < N2; j += kSelThreads) {
                 const uint32_t k = st_key[j];
                 if ((k >> kSub) == p19) {
                     const int s = atomicAdd(&sh.ntie, 1);
-                    if (s < 32)
-                        sh.tie[s] = key64(k, st_idx[j]);
+                    if (s < kMaxTie)
+                        tie[s] = key64(k, st_idx[j]);
                 }
             }
             __syncthreads();
-            if (sh.ntie <= 32) {
+            if (sh.ntie <= kMaxTie) {
                 if (warp == 0) {
                     const int nt = sh.ntie;
-                    const unsigned long long mine = lane < nt ? sh.tie[lane] : 0ull;
-                    int rk = 0;   // how many tied keys are larger
-                    for (int i = 0; i < nt; ++i)
-                        rk += sh.tie[i] > mine;
-                    if (lane < nt && rk == rem - 1)
-                        sh.tie_thr = mine;
+                    for (int q = 0; 32 * q < nt; ++q) {   // warp-uniform
+                        const int me = 32 * q + lane;
+                        const unsigned long long mine = me < nt ? tie[me] : 0ull;
+                        int rk = 0;   // how many tied keys are larger
+                        for (int i = 0; i < nt; ++i)
+                            rk += tie[i] > mine;
+                        if (me < nt && rk == rem - 1)
+                            sh.tie_thr = mine;
+                    }
                 }
                 __syncthreads();
             }
         }
-        thr = N2 <= need         ? 0ull
-              : sh.above2 < 0    ? staged_full_select(N2, need, st_idx, st_key, sh.sel)
-              : sh.ntie <= 32    ? sh.tie_thr
-                                 : staged_refine(N2, rem, p19, st_idx, st_key, sh.sel);
+        thr = N2 <= need           ? 0ull
+              : sh.above2 < 0      ? staged_full_select(N2, need, st_idx, st_key, sh.sel)
+              : sh.ntie <= kMaxTie ? sh.tie_thr
+                                   : staged_refine(N2, rem, p19, st_idx, st_key, sh.sel);
         n = stable_compact<kSelThreads, 4>(N2, thr, get_staged, w.K, sup_i, sup_k, sh.sel.warp_tot);
     } else {
         // more than kSelStageCap final candidates: select among all of them
