@@ -199,7 +199,7 @@ int retopk_decode_step_kv(retopk_ctx *ctx, const retopk_bf16 *k_new, const retop
  * [B, Hq, d], all bf16 on the host; k_cache, v_cache, d_seqlens stay on the
  * device.  Synchronous: returns once `out` holds the step's output.  The
  * inputs are copied into library-owned pinned, device-mapped memory; the
- * three kernels of retopk_decode_step_kv are replayed as a CUDA graph on
+ * kernels of retopk_decode_step_kv are replayed as a CUDA graph on
  * `stream` (captured on the first call and again whenever k_cache, v_cache or
  * d_seqlens change), the path-decision kernel reading the token's q, k_new,
  * v_new across the host link (and copying q to device memory for the later
