@@ -46,6 +46,13 @@ __global__ void __launch_bounds__(kSelThreads, 2) finish_kernel(SelArgs sa, Reus
         reuse_body<CL>(ra, fin_smem);
     else
         exact_select_body<CL>(sa, fin_smem);
+    // Reuse heads never wait for the grid before this one (the scan, or the
+    // exact-head prefilter), so on a step without exact heads nothing would.
+    // One CTA waiting before it exits keeps this grid from completing before
+    // that one: the next step's decision, which waits for this grid, then
+    // never overlaps a kernel of this step that still reads the paths.
+    if (blockIdx.x == 0 && blockIdx.y == 0)
+        pdl_wait();
 }
 
 size_t finish_smem_bytes_for(int max_len, int K, int RKW, int CL)
