@@ -230,6 +230,27 @@ def test_qwen_1m_prefilter_sampled():
     assert ((p != 0).sum() > 0) and (p[-3 * w.Hq:-2 * w.Hq] == 2).all()
 
 
+def test_prefiltered_heads_with_massive_ties():
+    # 160K keys: one repeated key row at every third position, zero rows
+    # elsewhere, so the history's scores take two values.  Exact heads at this
+    # length run the prefilter (two windows per CTA), and tens of thousands of
+    # keys share the 19-bit prefix: more final candidates than the select
+    # stages, so the window lists are compacted in place for the global
+    # select.  Every step against the oracle (ties to the lower index).
+    w = synth.scaled(synth.WORKLOADS["tiny_1h_2k"], L0=160_000, steps=6, Hq=4, K=512, tau=1.5, T_r=0,
+                     name="tiny_pf_ties")
+    arrays = synth.generate(w)
+    k = arrays[0]
+    row = k[0, 0, 1].copy()
+    k[:, :, :w.L0] = 0
+    k[:, :, :w.L0:3] = row
+    dr, errs, agg, paths = run_checked(w, arrays=arrays)
+    assert not errs, "\n".join(errs[:20])
+    assert (np.concatenate(paths) == 1).all()
+    diag = dr.ctx.retopk_get_diagnostics()
+    assert (diag["sup_len"] == w.K).all()
+
+
 def test_long_history_split_bitmap():
     # 3M keys: each rank's bitmap slice covers ~393K positions and the
     # retrieved supports spread over all of them
