@@ -32,6 +32,10 @@ __global__ void __launch_bounds__(kSelThreads, 2) finish_kernel(SelArgs sa, Reus
     // passed its own wait (the scan lets this grid launch only after that).
     // An exact head waits for the scan inside exact_select_body.
     const Work &w = sa.w;
+    // The next grid on the stream (the next step's or the next layer's
+    // decision) may launch now: it only prefetches before its own wait, which
+    // returns once this grid has completed.
+    pdl_trigger();
     if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y % w.Hq == 0) {
         // the ring advance of Eq. (5) (slot, live count, t_dec): nothing later
         // in this step reads `seq`, every head takes its slot from `snap`

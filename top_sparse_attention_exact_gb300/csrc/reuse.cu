@@ -40,6 +40,14 @@ struct DecideShared {
 __global__ void __launch_bounds__(kDecideThreads) decide_kernel(DecideArgs a)
 {
     __shared__ DecideShared sh;
+    {   // the head's cached queries (C rows of 256 bytes in the workspace)
+        // into the L2 while the grid before this one (the previous step's or
+        // layer's back end) finishes: a hint only, every value is read after
+        // the wait
+        const char *fq = reinterpret_cast<const char *>(a.w.fifo_q + (size_t)blockIdx.x * a.w.C * kD);
+        for (int i = threadIdx.x; i < a.w.C * kD * 2 / 128; i += kDecideThreads)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(fq + (size_t)i * 128));
+    }
     pdl_wait();      // the previous step is done with the caches, lengths and ring
     pdl_trigger();   // the scan may set up while the decision runs
     const Work &w = a.w;

@@ -12,6 +12,7 @@ template <int CL>
 __global__ void __launch_bounds__(kSelThreads, 2) exact_select_kernel(SelArgs a)
 {
     extern __shared__ __align__(128) unsigned char sel_smem[];
+    pdl_trigger();   // the next grid on the stream waits for this one before it reads anything
     exact_select_body<CL>(a, sel_smem);
 }
 
