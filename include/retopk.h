@@ -22,6 +22,13 @@
  *     synchronises the device (except where stated: create, init, export,
  *     import, status and counter reads) and never allocates device memory:
  *     the caller provides the workspace.
+ *   - The library's kernels use programmatic dependent launch among
+ *     themselves, and the last kernel of a decode or exact step lets the next
+ *     grid on the stream launch before it completes.  A plain launch after a
+ *     call is ordered as usual; a kernel the caller launches with
+ *     programmatic stream serialisation behind a call must wait for its grid
+ *     dependency (griddepcontrol.wait / cudaGridDependencySynchronize) before
+ *     it reads the call's outputs.
  *   - Return value: RETOPK_OK (0) or a negative RETOPK_ERR_* code.  Argument
  *     errors are detected on the host before anything is launched.  Faults the
  *     device detects (an out-of-range support index in the cache, a full KV
