@@ -23,8 +23,8 @@
  *     import, status and counter reads) and never allocates device memory:
  *     the caller provides the workspace.
  *   - The library's kernels use programmatic dependent launch among
- *     themselves, and the last kernel of a decode or exact step lets the next
- *     grid on the stream launch before it completes.  A plain launch after a
+ *     themselves, and the last kernel of a call may let the next grid on the
+ *     stream launch before it completes.  A plain launch after a
  *     call is ordered as usual; a kernel the caller launches with
  *     programmatic stream serialisation behind a call must wait for its grid
  *     dependency (griddepcontrol.wait / cudaGridDependencySynchronize) before
